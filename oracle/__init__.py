@@ -1,0 +1,4 @@
+"""CPU oracle (test infrastructure only): fp64 restatement of the unmerged multi-adapter LoRA layer."""
+from .lora_oracle import (OK, EINVAL, ENOPAGES, EUNKNOWN_ADAPTER, ERANK, EEXIST, MAX_RANK,  # noqa: F401
+                          PoolModel, bf16_to_f64, bf16_round, gather_adapter, linear_forward, place_adapter,
+                          merged_forward, segments)

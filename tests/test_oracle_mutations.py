@@ -1,0 +1,111 @@
+"""Plant plausible mistakes in a copy of the oracle; the pins must catch each one (CPU only)."""
+import types
+
+import numpy as np
+import pytest
+
+import oracle as O
+from oracle import lora_oracle as L
+from pins import ALL_PINS
+
+
+def _forward(mut):
+    """The oracle's forward with one planted mistake, selected by ``mut``."""
+    def linear_forward(pool_bits, tables, token_adapter, slot, x_bits, Wt_bits, tokens=None):
+        ta = np.asarray(token_adapter, dtype=np.int64)
+        idx = np.arange(ta.size) if tokens is None else np.asarray(tokens, dtype=np.int64)
+        x = L.bf16_to_f64(x_bits[idx])
+        W = L.bf16_to_f64(Wt_bits) if mut == "W_not_transposed" else L.bf16_to_f64(Wt_bits).T
+        base = x @ W
+        delta = np.zeros_like(base)
+        for row, t in enumerate(idx):
+            a = int(ta[t])
+            if a < 0:
+                continue
+            if mut == "neighbour_adapter":
+                a = (a + 1) % len(tables)
+            tab = tables[a][0 if mut == "slot_ignored" else slot]
+            if tab[0, 0] < 0:
+                continue
+            if mut == "A_B_pages_swapped":
+                A, B = L.bf16_to_f64(pool_bits[tab[1]]).T, L.bf16_to_f64(pool_bits[tab[0]])
+            elif mut == "A_pages_reversed":
+                A, B = L.bf16_to_f64(pool_bits[tab[0][::-1]]).T, L.bf16_to_f64(pool_bits[tab[1]])
+            else:
+                A, B = L.gather_adapter(pool_bits, tab)
+            if mut == "last_rank_dropped":
+                A, B = A[:, :-1], B[:-1]
+            delta[row] = (x[row] @ A) @ B
+        if mut == "lora_dropped":
+            delta[:] = 0
+        if mut == "lora_sign":
+            return base - delta, -delta
+        return base + delta, delta
+    return linear_forward
+
+
+def _segments_unstable(token_adapter):
+    ta = np.asarray(token_adapter, dtype=np.int64)
+    perm, off, sa = L.segments(ta)
+    perm = perm.copy()
+    for s in range(len(sa)):
+        perm[off[s]:off[s + 1]] = perm[off[s]:off[s + 1]][::-1]     # ties in descending token order
+    return perm, off, sa
+
+
+def _segments_none_last(token_adapter):
+    ta = np.asarray(token_adapter, dtype=np.int64)
+    key = np.where(ta < 0, np.iinfo(np.int64).max, ta)
+    perm = np.argsort(key, kind="stable")
+    perm2, off, sa = L.segments(ta)
+    return perm.astype(np.int32), off, sa
+
+
+def _place_swapped(pool_bits, table, A_list, B_list):
+    for s, (A, B) in enumerate(zip(A_list, B_list)):
+        if A is None:
+            continue
+        for j in range(A.shape[1]):
+            pool_bits[table[s, 1, j]] = A[:, j]
+            pool_bits[table[s, 0, j]] = B[j, :]
+
+
+class _PoolFrontPop(L.PoolModel):
+    def load(self, adapter, rank, present):
+        self.free.reverse()
+        try:
+            return super().load(adapter, rank, present)
+        finally:
+            self.free.reverse()
+
+
+MUTANTS = {
+    "lora_dropped": dict(linear_forward=_forward("lora_dropped")),
+    "lora_sign": dict(linear_forward=_forward("lora_sign")),
+    "W_not_transposed": dict(linear_forward=_forward("W_not_transposed")),
+    "A_B_pages_swapped": dict(linear_forward=_forward("A_B_pages_swapped")),
+    "A_pages_reversed": dict(linear_forward=_forward("A_pages_reversed")),
+    "last_rank_dropped": dict(linear_forward=_forward("last_rank_dropped")),
+    "slot_ignored": dict(linear_forward=_forward("slot_ignored")),
+    "neighbour_adapter": dict(linear_forward=_forward("neighbour_adapter")),
+    "segments_unstable": dict(segments=_segments_unstable),
+    "segments_none_last": dict(segments=_segments_none_last),
+    "place_swapped": dict(place_adapter=_place_swapped),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    mutant = types.SimpleNamespace(**{k: getattr(O, k) for k in dir(O) if not k.startswith("_")})
+    for k, v in MUTANTS[name].items():
+        setattr(mutant, k, v)
+    failed = [p.__name__ for p in ALL_PINS if not p(mutant)[0]]
+    assert failed, f"no pin caught mutant {name}"
+
+
+def test_front_pop_changes_tables_but_not_outputs():
+    """Popping from the wrong end is invisible to the forward (placement invariance) but
+    changes the page tables, which the GPU parity tests compare bit-exactly."""
+    a = L.PoolModel(20, 1, 2, page_order=np.arange(20))
+    b = _PoolFrontPop(20, 1, 2, page_order=np.arange(20))
+    assert not np.array_equal(a.load(0, 3, [True])[1], b.load(0, 3, [True])[1])

@@ -1,0 +1,102 @@
+"""The oracle against what the pages and the mathematics fix (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads
+from pins import ALL_PINS, build_scene
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_pin_holds(pin):
+    ok, msg = pin(O)
+    assert ok, msg
+
+
+def test_worked_example_page_arithmetic():
+    """'Unified paging' worked example: adapter and KV sizes in pages and bytes."""
+    g = json.load(open(os.path.join(GOLDEN, "pool_worked_example.json")))
+    H, L, nb = g["hidden"], g["layers"], g["bytes_per_value"]
+    kv_vectors = 2 * L                                       # K and V per layer
+    assert kv_vectors == g["kv_vectors_per_token"]
+    assert kv_vectors * H * nb == g["kv_bytes_per_token"]
+    assert g["adapter_rank"] * 2 * g["projections"] == g["adapter_vectors_per_layer"]
+    pages = O.PoolModel.pages_for_adapter(g["adapter_rank"], L, g["projections"])
+    assert pages == g["adapter_vectors"]
+    assert pages * H * nb == g["adapter_bytes"]
+    assert g["adapter_bytes"] // g["kv_bytes_per_token"] == g["kv_tokens_per_adapter"]
+    assert round(g["context_tokens"] / g["kv_tokens_per_adapter"]) == g["adapters_per_context_about"]
+    total_gib = g["adapters"] * g["adapter_bytes"] / 2**30
+    assert abs(total_gib - g["adapters_total_gib_about"]) < 1.0
+
+
+def test_pool_enopages_exactly_at_boundary_and_unchanged():
+    pool = O.PoolModel(100, n_slots=2, max_adapters=8, page_order=np.random.default_rng(0).permutation(100))
+    assert pool.reserve(36)[0] == O.OK                       # 64 left
+    assert pool.load(0, 16, [True, True])[0] == O.OK          # 64 pages -> 0 left
+    before = (list(pool.free), dict(pool.ranks))
+    assert pool.load(1, 1, [True, False])[0] == O.ENOPAGES    # needs 2, has 0
+    assert (list(pool.free), dict(pool.ranks)) == before
+    assert pool.unload(0) == O.OK
+    st, tab = pool.load(1, 16, [True, True])                 # exactly 64 again
+    assert st == O.OK and len(pool.free) == 0
+    assert pool.load(2, 1, [True, False])[0] == O.ENOPAGES
+
+
+def test_pool_errors_and_stats():
+    pool = O.PoolModel(64, n_slots=3, max_adapters=4)
+    assert pool.load(0, 0, [True] * 3)[0] == O.ERANK
+    assert pool.load(0, 65, [True] * 3)[0] == O.ERANK
+    assert pool.load(4, 8, [True] * 3)[0] == O.EINVAL
+    assert pool.load(-1, 8, [True] * 3)[0] == O.EINVAL
+    assert pool.load(1, 8, [True, False, True])[0] == O.OK
+    assert pool.load(1, 8, [True] * 3)[0] == O.EEXIST
+    assert pool.unload(2) == O.EUNKNOWN_ADAPTER
+    st, ids = pool.reserve(5)
+    assert pool.release(ids + [ids[0]]) == O.EINVAL           # duplicate
+    assert pool.stats() == {"free": 64 - 32 - 5, "adapter": 32, "reserved": 5, "resident_adapters": 1}
+    assert pool.release(ids) == O.OK
+    assert pool.tables[1][1].min() == -1 and pool.tables[1][0].min() >= 0
+
+
+def test_free_list_pops_from_end_in_table_order():
+    order = np.array([5, 9, 2, 7, 1, 0, 3, 8, 4, 6])
+    pool = O.PoolModel(10, n_slots=2, max_adapters=2, page_order=order)
+    st, tab = pool.load(0, 2, [True, True])
+    assert st == O.OK
+    # slot 0: A pages then B pages, then slot 1; each taken from the end of the list
+    assert tab.reshape(-1).tolist() == [6, 4, 8, 3, 0, 1, 7, 2]
+
+
+def test_init_statistics_unit_variance():
+    """With x~N(0,1), W,A~N(0,1/H), B~N(0,1/r): x W and the delta have variance near 1."""
+    sc = build_scene(O, H=256, ranks=[16], T=64, seed=21, none_share=0.0)
+    y, delta = O.linear_forward(sc["pool_bits"], sc["pool"].tables, sc["ta"], 0, sc["x"], sc["Wt"][0])
+    base = y - delta
+    assert 0.7 < base.var() < 1.3
+    assert 0.6 < delta.var() < 1.4
+
+
+def test_workload_structure():
+    w2 = workloads.make(2)
+    assert w2.T == 256 and w2.ranks.shape == (64,) and set(np.unique(w2.ranks)) <= {8, 16, 32, 64}
+    w3 = workloads.make(3)
+    assert len(set(w3.req_adapter.tolist())) == 16 and 16 * 128 <= w3.T <= 16 * 1024
+    w1 = workloads.make(1)
+    assert w1.T == 32 and w1.ranks.tolist() == [8, 8, 16, 16]
+    for k in (1, 2, 3, 4, 5):
+        w = workloads.make(k)
+        assert w.adapter_pages() + w.kv_pages <= w.spec.pool_pages
+    # lazily drawn tensors are reproducible one by one
+    assert np.array_equal(w2.A(3, 1), workloads.make(2).A(3, 1))
+
+
+def test_bf16_round_ties_to_even():
+    vals = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, 256.0, -3.5])
+    got = O.bf16_round(vals)
+    assert got.tolist() == [1.0, 1.0, 1.0 + 2**-6, 256.0, -3.5]
