@@ -1,0 +1,238 @@
+"""GB300 multi-adapter LoRA projection: Python binding over liblora.so (C ABI in include/lora.h).
+
+Every function here has the name of the C entry point it wraps and only
+marshals arguments: device pointers may be given as ints or as objects with a
+``data_ptr()`` method (PyTorch tensors), host arrays as NumPy arrays, streams
+as ``cudaStream_t`` ints (default: PyTorch's current stream).  A non-zero
+status raises :class:`LoraError` carrying the code and ``lora_last_error()``.
+
+The library must be built first (``adapter_gemm_lora_gb300.build.build()``);
+there is no fallback implementation: if the shared library is missing, loading
+it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "liblora.so")
+
+LORA_OK = 0
+LORA_EINVAL = -1
+LORA_ENOPAGES = -2
+LORA_EUNKNOWN_ADAPTER = -3
+LORA_ERANK = -4
+LORA_EEXIST = -5
+LORA_ECUDA = -6
+LORA_EDEVICE = -7
+LORA_MAX_RANK = 64
+LORA_MAX_ADAPTERS = 16384
+LORA_MAX_TOKENS = 65536
+
+EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_adapter_load",
+            "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",
+            "lora_linear_forward", "lora_status", "lora_pool_stats", "lora_last_error", "lora_pool_destroy",
+            "lora_profile_enable", "lora_profile_read"]
+KINDS = ("segments", "shrink", "expand", "gemm", "scatter")
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+        self.message = message
+
+
+class lora_segments(ctypes.Structure):
+    _fields_ = [("T_max", ctypes.c_int32), ("T", ctypes.c_int32), ("max_seg", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("perm", ctypes.c_void_p), ("seg_off", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
+                ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("shrink_work", ctypes.c_void_p),
+                ("n_shrink", ctypes.c_void_p), ("expand_work", ctypes.c_void_p), ("n_expand", ctypes.c_void_p),
+                ("shrink_cap", ctypes.c_int32), ("expand_cap", ctypes.c_int32),
+                ("s", ctypes.c_void_p), ("delta", ctypes.c_void_p)]
+
+
+class lora_pool_stats_t(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int64), ("free_pages", ctypes.c_int64), ("adapter_pages", ctypes.c_int64),
+                ("reserved_pages", ctypes.c_int64), ("resident_adapters", ctypes.c_int32),
+                ("max_adapters", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = os.environ.get("LORA_LIB", LIB_PATH)
+    if not os.path.exists(path):
+        raise RuntimeError(f"liblora.so not found at {path}; build it with adapter_gemm_lora_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    sig = {
+        "lora_pool_create": (I32, [VP, I64, I32, I32, I32, VP, P(VP)]),
+        "lora_pool_reserve": (I32, [VP, I64, VP]),
+        "lora_pool_release": (I32, [VP, I64, VP]),
+        "lora_adapter_load": (I32, [VP, I32, I32, VP, VP, VP, VP]),
+        "lora_adapter_unload": (I32, [VP, I32, VP]),
+        "lora_segments_size": (I64, [VP, I32]),
+        "lora_segments_init": (I32, [VP, VP, I64, I32, P(lora_segments)]),
+        "lora_segments_build": (I32, [VP, VP, I32, P(lora_segments), VP]),
+        "lora_linear_forward": (I32, [VP, P(lora_segments), I32, VP, VP, VP, VP, VP]),
+        "lora_status": (I32, [VP, VP]),
+        "lora_pool_stats": (None, [VP, P(lora_pool_stats_t)]),
+        "lora_last_error": (ctypes.c_char_p, []),
+        "lora_pool_destroy": (None, [VP]),
+        "lora_profile_enable": (I32, [VP, I32]),
+        "lora_profile_read": (I32, [VP, I32, VP, VP, I32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def library():
+    """The loaded ctypes library (loads it on first use)."""
+    return _load()
+
+
+def _ptr(obj) -> Optional[int]:
+    if obj is None:
+        return None
+    if isinstance(obj, int):
+        return obj
+    if hasattr(obj, "data_ptr"):
+        return obj.data_ptr()
+    if isinstance(obj, np.ndarray):
+        return obj.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(obj)!r}")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return int(stream) if not hasattr(stream, "cuda_stream") else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(rc: int) -> None:
+    if rc != LORA_OK:
+        raise LoraError(rc, lora_last_error())
+
+
+def lora_last_error() -> str:
+    return _load().lora_last_error().decode()
+
+
+def lora_pool_create(pool_dev, num_pages: int, H: int, n_slots: int, max_adapters: int,
+                     page_order: Optional[np.ndarray] = None) -> ctypes.c_void_p:
+    """Create a pool over device bf16 storage [num_pages][H] (None: planning pool)."""
+    order = None if page_order is None else np.ascontiguousarray(page_order, dtype=np.int64)
+    out = ctypes.c_void_p()
+    _check(_load().lora_pool_create(_ptr(pool_dev), num_pages, H, n_slots, max_adapters, _ptr(order),
+                                    ctypes.byref(out)))
+    return out
+
+
+def lora_pool_reserve(pool, n: int) -> np.ndarray:
+    ids = np.zeros(max(n, 1), dtype=np.int64)
+    _check(_load().lora_pool_reserve(pool, n, _ptr(ids)))
+    return ids[:n]
+
+
+def lora_pool_release(pool, ids) -> None:
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    _check(_load().lora_pool_release(pool, ids.size, _ptr(ids) if ids.size else None))
+
+
+def lora_adapter_load(pool, adapter_id: int, rank: int, A_host: Optional[Sequence], B_host: Optional[Sequence],
+                      n_slots: int, stream=None, planning: bool = False) -> np.ndarray:
+    """Load one adapter; A_host[slot] bf16 bits [H, rank] (None: no LoRA there), B_host[slot] [rank, H].
+
+    Returns the page table int32 [n_slots, 2, rank].
+    """
+    keep = []
+
+    def arr(seq):
+        if seq is None:
+            return None
+        a = (ctypes.c_void_p * n_slots)()
+        for i, m in enumerate(seq):
+            if m is None:
+                a[i] = None
+            else:
+                m = np.ascontiguousarray(m, dtype=np.uint16)
+                keep.append(m)
+                a[i] = m.ctypes.data
+        return a
+
+    a_arr, b_arr = arr(A_host), arr(B_host)
+    table = np.zeros((n_slots, 2, rank), dtype=np.int32)
+    st = 0 if planning else _stream(stream)
+    rc = _load().lora_adapter_load(pool, adapter_id, rank, ctypes.cast(a_arr, ctypes.c_void_p) if a_arr else None,
+                                   ctypes.cast(b_arr, ctypes.c_void_p) if b_arr else None, st, _ptr(table))
+    _check(rc)
+    return table
+
+
+def lora_adapter_unload(pool, adapter_id: int, stream=None, planning: bool = False) -> None:
+    _check(_load().lora_adapter_unload(pool, adapter_id, 0 if planning else _stream(stream)))
+
+
+def lora_segments_size(pool, T_max: int) -> int:
+    n = _load().lora_segments_size(pool, T_max)
+    if n < 0:
+        raise LoraError(int(n), lora_last_error())
+    return int(n)
+
+
+def lora_segments_init(pool, workspace_dev, workspace_bytes: int, T_max: int) -> lora_segments:
+    seg = lora_segments()
+    _check(_load().lora_segments_init(pool, _ptr(workspace_dev), workspace_bytes, T_max, ctypes.byref(seg)))
+    return seg
+
+
+def lora_segments_build(pool, token_adapter_dev, T: int, seg: lora_segments, stream=None) -> None:
+    _check(_load().lora_segments_build(pool, _ptr(token_adapter_dev), T, ctypes.byref(seg), _stream(stream)))
+
+
+def lora_linear_forward(pool, seg: lora_segments, slot: int, x_dev, W_dev, y_dev, delta_dbg_dev=None,
+                        stream=None) -> None:
+    _check(_load().lora_linear_forward(pool, ctypes.byref(seg), slot, _ptr(x_dev), _ptr(W_dev), _ptr(y_dev),
+                                       _ptr(delta_dbg_dev), _stream(stream)))
+
+
+def lora_status(pool, stream=None) -> None:
+    _check(_load().lora_status(pool, _stream(stream)))
+
+
+def lora_pool_stats(pool) -> dict:
+    s = lora_pool_stats_t()
+    _load().lora_pool_stats(pool, ctypes.byref(s))
+    return {"num_pages": s.num_pages, "free": s.free_pages, "adapter": s.adapter_pages,
+            "reserved": s.reserved_pages, "resident_adapters": s.resident_adapters, "max_adapters": s.max_adapters}
+
+
+def lora_pool_destroy(pool) -> None:
+    _load().lora_pool_destroy(pool)
+
+
+def lora_profile_enable(pool, enable: bool = True) -> None:
+    _check(_load().lora_profile_enable(pool, 1 if enable else 0))
+
+
+def lora_profile_read(pool, reset: bool = True) -> dict:
+    """Per kernel kind: launches and summed device ms of the recorded launches."""
+    n = len(KINDS)
+    launches = np.zeros(n, dtype=np.int64)
+    ms = np.zeros(n, dtype=np.float64)
+    _check(_load().lora_profile_read(pool, n, _ptr(launches), _ptr(ms), 1 if reset else 0))
+    return {k: {"launches": int(launches[i]), "ms": float(ms[i])} for i, k in enumerate(KINDS)}

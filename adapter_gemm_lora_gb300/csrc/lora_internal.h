@@ -1,0 +1,107 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/lora.h"
+
+// Device error word layout (int32[4]): [0] first error code (LORA_E*), [1] detail bits.
+enum : int32_t {
+  LORA_DEV_UNKNOWN_ADAPTER = 1 << 0,   // token id out of range or not loaded
+  LORA_DEV_BAD_PAGE = 1 << 1,          // page id outside [0, num_pages)
+  LORA_DEV_BAD_RANK = 1 << 2,          // rank outside [1, 64]
+  LORA_DEV_WAIT_TIMEOUT = 1 << 3,      // a bounded mbarrier wait gave up
+  LORA_DEV_BAD_SEGMENT = 1 << 4,       // inconsistent segment / work list
+};
+
+// Page table entries per (adapter, slot): [2][LORA_MAX_RANK] int32.
+constexpr int kTabStride = 2 * LORA_MAX_RANK;
+
+struct lora_pool {
+  void* pool_dev = nullptr;
+  int64_t num_pages = 0;
+  int32_t H = 0;
+  int32_t n_slots = 0;
+  int32_t max_adapters = 0;
+  bool planning = false;
+  int device = -1;
+
+  // host bookkeeping
+  std::vector<int32_t> free_list;                 // taken from the back
+  std::vector<uint8_t> page_state;                // 0 free, 1 reserved, 2 adapter
+  std::vector<int32_t> rank;                      // per adapter id; 0 = not loaded
+  std::vector<std::vector<int32_t>> tables;       // per adapter id: [n_slots][2][rank]
+  int64_t adapter_pages = 0;
+  int64_t reserved_pages = 0;
+  int32_t resident = 0;
+
+  // device state owned by the library
+  int32_t* d_ptab = nullptr;    // [max_adapters][n_slots][2][64]
+  int32_t* d_rank = nullptr;    // [max_adapters]
+  int32_t* d_err = nullptr;     // [4]
+  void* d_stage = nullptr;      // staging area for adapter loads
+  size_t d_stage_bytes = 0;
+  std::vector<uint16_t> h_stage;
+
+  // kernel accounting (lora_profile_*)
+  int64_t launches[LORA_N_KINDS] = {0, 0, 0, 0, 0};
+  bool prof_on = false;
+  struct ProfRec { int kind; cudaEvent_t start, stop; };
+  std::vector<ProfRec> prof_rec;
+  std::vector<cudaEvent_t> ev_free;
+};
+
+// Bracket one kernel launch: count it and, when profiling is on, record events around it.
+struct ProfScope {
+  lora_pool* p;
+  int kind;
+  cudaStream_t st;
+  int rec = -1;
+  ProfScope(const lora_pool* pool, int k, cudaStream_t s);
+  ~ProfScope();
+};
+
+// Error reporting (thread-local message).
+int lora_fail(int code, const std::string& msg);
+int lora_cuda_fail(cudaError_t e, const char* what);
+
+// Kernel launchers (return LORA_OK or LORA_ECUDA).
+int launch_scatter_pages(const uint16_t* stage, const int32_t* d_pages, int64_t n_pages, int32_t H,
+                         void* pool_dev, cudaStream_t st);
+int launch_segments_build(const lora_pool* pool, const int32_t* token_adapter, int32_t T,
+                          const lora_segments* seg, cudaStream_t st);
+
+struct LoraLaunch {
+  const uint16_t* pool;
+  int64_t num_pages;
+  int32_t H, T, slot, n_slots;
+  const int32_t* ptab;
+  const int32_t* rank;
+  const lora_segments* seg;
+  const uint16_t* x;
+  float* delta;
+  int32_t* err;
+};
+int launch_shrink(const LoraLaunch& L, cudaStream_t st);
+int launch_expand(const LoraLaunch& L, cudaStream_t st);
+
+struct GemmLaunch {
+  const uint16_t* x;       // [T][H]
+  const uint16_t* W;       // [H][H] (out, in)
+  uint16_t* y;             // [T][H]
+  const float* delta;      // [T][H]
+  const int32_t* tok_adapter;  // [T] validated ids
+  const int32_t* ptab;
+  int32_t T, H, slot, n_slots;
+  int32_t* err;
+};
+int launch_gemm(const GemmLaunch& G, cudaStream_t st);
+
+// Work-list geometry shared by the segment builder and the gather kernels.
+constexpr int kShrinkTokBlock = 8;   // tokens per shrink unit
+constexpr int kShrinkRankGroup = 8;  // rank columns per shrink unit
+constexpr int kExpandTokBlock = 8;   // tokens per expand unit

@@ -1,0 +1,448 @@
+// Unified page pool: host bookkeeping, device page tables, adapter loading, status.
+//
+// "S-LoRA, in depth", section "Unified paging: adapters and KV cache in one pool":
+// one page holds one H-vector; KV cache and adapters draw pages from one free list;
+// a rank-r A or B takes r pages.  The pool sketch there pops its free list from the
+// end and appends freed pages; this pool keeps that order so that page placement is
+// reproducible from the initial free-list order.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "lora_internal.h"
+
+namespace {
+thread_local std::string g_last_error;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Copy staged rows (page ids first, then the rows in the same order) into their pages.
+__global__ void scatter_pages_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ rows,
+                                     int64_t n_pages, int32_t H, uint4* __restrict__ pool) {
+  const int64_t vec_per_row = H / 8;   // 8 bf16 per 16-byte vector
+  for (int64_t r = blockIdx.x; r < n_pages; r += gridDim.x) {
+    const int64_t page = ids[r];
+    const uint4* src = rows + r * vec_per_row;
+    uint4* dst = pool + page * vec_per_row;
+    for (int64_t v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = src[v];
+  }
+}
+}  // namespace
+
+int lora_fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int lora_cuda_fail(cudaError_t e, const char* what) {
+  return lora_fail(LORA_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+int launch_scatter_pages(const uint16_t* stage, const int32_t* d_pages, int64_t n_pages, int32_t H,
+                         void* pool_dev, cudaStream_t st) {
+  (void)stage;
+  if (n_pages == 0) return LORA_OK;
+  const size_t ids_bytes = align_up(n_pages * sizeof(int32_t), 256);
+  const uint4* rows = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(d_pages) + ids_bytes);
+  int grid = (int)std::min<int64_t>(n_pages, 4096);
+  scatter_pages_kernel<<<grid, 256, 0, st>>>(d_pages, rows, n_pages, H, reinterpret_cast<uint4*>(pool_dev));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "scatter_pages launch");
+}
+
+namespace {
+cudaEvent_t take_event(lora_pool* p) {
+  if (!p->ev_free.empty()) {
+    cudaEvent_t e = p->ev_free.back();
+    p->ev_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(const lora_pool* pool, int k, cudaStream_t s) : p(const_cast<lora_pool*>(pool)), kind(k), st(s) {
+  p->launches[kind] += 1;
+  if (!p->prof_on) return;
+  cudaEvent_t a = take_event(p), b = take_event(p);
+  if (!a || !b) return;
+  // External records also become event nodes when the stream is being captured into a graph.
+  cudaEventRecordWithFlags(a, st, cudaEventRecordExternal);
+  p->prof_rec.push_back({kind, a, b});
+  rec = (int)p->prof_rec.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (rec >= 0) cudaEventRecordWithFlags(p->prof_rec[rec].stop, st, cudaEventRecordExternal);
+}
+
+extern "C" {
+
+const char* lora_last_error(void) { return g_last_error.c_str(); }
+
+int lora_profile_enable(lora_pool* p, int32_t enable) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_profile_enable: pool is NULL");
+  if (p->planning && enable) return lora_fail(LORA_EINVAL, "lora_profile_enable: planning pool launches nothing");
+  p->prof_on = enable != 0;
+  return LORA_OK;
+}
+
+int lora_profile_read(lora_pool* p, int32_t n_kinds, int64_t* launches, double* ms, int32_t reset) {
+  if (!p || n_kinds < 0 || (n_kinds > 0 && (!launches || !ms))) return lora_fail(LORA_EINVAL, "lora_profile_read: bad arguments");
+  double acc[LORA_N_KINDS] = {0, 0, 0, 0, 0};
+  int rc = LORA_OK;
+  for (auto& r : p->prof_rec) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e != cudaSuccess && rc == LORA_OK) rc = lora_cuda_fail(e, "lora_profile_read");
+    acc[r.kind] += t;
+  }
+  for (int k = 0; k < n_kinds; ++k) {
+    launches[k] = k < LORA_N_KINDS ? p->launches[k] : 0;
+    ms[k] = k < LORA_N_KINDS ? acc[k] : 0.0;
+  }
+  if (reset) {
+    for (auto& r : p->prof_rec) {
+      p->ev_free.push_back(r.start);
+      p->ev_free.push_back(r.stop);
+    }
+    p->prof_rec.clear();
+    for (int k = 0; k < LORA_N_KINDS; ++k) p->launches[k] = 0;
+  }
+  return rc;
+}
+
+int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slots, int32_t max_adapters,
+                     const int64_t* page_order_host, lora_pool** out) {
+  if (!out) return lora_fail(LORA_EINVAL, "lora_pool_create: out is NULL");
+  *out = nullptr;
+  if (num_pages < 1 || num_pages > INT32_MAX)
+    return lora_fail(LORA_EINVAL, "lora_pool_create: num_pages must be in [1, 2^31-1]");
+  if (H < 64 || H > 16384 || H % 64 != 0)
+    return lora_fail(LORA_EINVAL, "lora_pool_create: H must be a multiple of 64 in [64, 16384]");
+  if (n_slots < 1) return lora_fail(LORA_EINVAL, "lora_pool_create: n_slots must be >= 1");
+  if (max_adapters < 1 || max_adapters > LORA_MAX_ADAPTERS)
+    return lora_fail(LORA_EINVAL, "lora_pool_create: max_adapters must be in [1, LORA_MAX_ADAPTERS]");
+  if ((reinterpret_cast<uintptr_t>(pool_dev) & 15) != 0)
+    return lora_fail(LORA_EINVAL, "lora_pool_create: pool storage must be 16-byte aligned");
+
+  lora_pool* p = new (std::nothrow) lora_pool();
+  if (!p) return lora_fail(LORA_EINVAL, "lora_pool_create: out of host memory");
+  p->pool_dev = pool_dev;
+  p->num_pages = num_pages;
+  p->H = H;
+  p->n_slots = n_slots;
+  p->max_adapters = max_adapters;
+  p->planning = (pool_dev == nullptr);
+  p->page_state.assign(num_pages, 0);
+  p->free_list.resize(num_pages);
+  if (page_order_host) {
+    std::vector<uint8_t> seen(num_pages, 0);
+    for (int64_t i = 0; i < num_pages; ++i) {
+      const int64_t v = page_order_host[i];
+      if (v < 0 || v >= num_pages || seen[v]) {
+        delete p;
+        return lora_fail(LORA_EINVAL, "lora_pool_create: page_order is not a permutation of 0..num_pages-1");
+      }
+      seen[v] = 1;
+      p->free_list[i] = (int32_t)v;
+    }
+  } else {
+    for (int64_t i = 0; i < num_pages; ++i) p->free_list[i] = (int32_t)i;
+  }
+  p->rank.assign(max_adapters, 0);
+  p->tables.resize(max_adapters);
+
+  if (!p->planning) {
+    cudaError_t e = cudaGetDevice(&p->device);
+    const size_t tab_bytes = (size_t)max_adapters * n_slots * kTabStride * sizeof(int32_t);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_ptab, tab_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_rank, (size_t)max_adapters * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_err, 4 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(p->d_ptab, 0xFF, tab_bytes);
+    if (e == cudaSuccess) e = cudaMemset(p->d_rank, 0, (size_t)max_adapters * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, 4 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      lora_pool_destroy(p);
+      return lora_cuda_fail(e, "lora_pool_create");
+    }
+  }
+  *out = p;
+  return LORA_OK;
+}
+
+void lora_pool_destroy(lora_pool* p) {
+  if (!p) return;
+  for (auto& r : p->prof_rec) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  for (auto e : p->ev_free) cudaEventDestroy(e);
+  if (p->d_ptab) cudaFree(p->d_ptab);
+  if (p->d_rank) cudaFree(p->d_rank);
+  if (p->d_err) cudaFree(p->d_err);
+  if (p->d_stage) cudaFree(p->d_stage);
+  delete p;
+}
+
+int lora_pool_reserve(lora_pool* p, int64_t n, int64_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return lora_fail(LORA_EINVAL, "lora_pool_reserve: bad arguments");
+  if (n > (int64_t)p->free_list.size())
+    return lora_fail(LORA_ENOPAGES, "lora_pool_reserve: " + std::to_string(n) + " pages asked, " +
+                                        std::to_string(p->free_list.size()) + " free");
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t pg = p->free_list.back();
+    p->free_list.pop_back();
+    p->page_state[pg] = 1;
+    ids[i] = pg;
+  }
+  p->reserved_pages += n;
+  return LORA_OK;
+}
+
+int lora_pool_release(lora_pool* p, int64_t n, const int64_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return lora_fail(LORA_EINVAL, "lora_pool_release: bad arguments");
+  int64_t i = 0;
+  for (; i < n; ++i) {   // validate, marking as we go so duplicates are caught
+    const int64_t pg = ids[i];
+    if (pg < 0 || pg >= p->num_pages || p->page_state[pg] != 1) break;
+    p->page_state[pg] = 3;
+  }
+  if (i < n) {
+    for (int64_t k = 0; k < i; ++k) p->page_state[ids[k]] = 1;
+    return lora_fail(LORA_EINVAL, "lora_pool_release: page " + std::to_string(ids[i]) +
+                                      " is not reserved or is listed twice");
+  }
+  for (int64_t k = 0; k < n; ++k) {
+    p->page_state[ids[k]] = 0;
+    p->free_list.push_back((int32_t)ids[k]);
+  }
+  p->reserved_pages -= n;
+  return LORA_OK;
+}
+
+int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const* A_host,
+                      const void* const* B_host, lora_stream_t stream, int32_t* table_out) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_load: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters)
+    return lora_fail(LORA_EINVAL, "lora_adapter_load: adapter id " + std::to_string(aid) + " outside [0, max_adapters)");
+  if (rank < 1 || rank > LORA_MAX_RANK)
+    return lora_fail(LORA_ERANK, "lora_adapter_load: rank " + std::to_string(rank) + " outside [1, 64]");
+  if (p->rank[aid] != 0) return lora_fail(LORA_EEXIST, "lora_adapter_load: adapter " + std::to_string(aid) + " already loaded");
+  if (!p->planning && (!A_host || !B_host))
+    return lora_fail(LORA_EINVAL, "lora_adapter_load: A_host and B_host arrays are required");
+  const int S = p->n_slots;
+  std::vector<uint8_t> present(S, 1);
+  if (A_host)
+    for (int s = 0; s < S; ++s) present[s] = A_host[s] != nullptr;
+  if (!p->planning)
+    for (int s = 0; s < S; ++s)
+      if (present[s] && !B_host[s]) return lora_fail(LORA_EINVAL, "lora_adapter_load: B_host[slot] is NULL where A_host[slot] is set");
+  int64_t n_present = 0;
+  for (int s = 0; s < S; ++s) n_present += present[s];
+  const int64_t need = 2 * (int64_t)rank * n_present;
+  if (need > (int64_t)p->free_list.size())
+    return lora_fail(LORA_ENOPAGES, "lora_adapter_load: adapter needs " + std::to_string(need) + " pages, " +
+                                        std::to_string(p->free_list.size()) + " free");
+
+  // Take pages: slot-major, A then B, j ascending, each from the end of the free list.
+  std::vector<int32_t> table((size_t)S * 2 * rank, -1);
+  std::vector<int32_t> taken;
+  taken.reserve(need);
+  for (int s = 0; s < S; ++s) {
+    if (!present[s]) continue;
+    for (int half = 0; half < 2; ++half)
+      for (int j = 0; j < rank; ++j) {
+        const int32_t pg = p->free_list.back();
+        p->free_list.pop_back();
+        table[((size_t)s * 2 + half) * rank + j] = pg;
+        taken.push_back(pg);
+      }
+  }
+  auto rollback = [&]() {
+    for (auto it = taken.rbegin(); it != taken.rend(); ++it) p->free_list.push_back(*it);
+  };
+
+  if (!p->planning) {
+    const int64_t H = p->H;
+    const size_t ids_bytes = align_up(need * sizeof(int32_t), 256);
+    const size_t bytes = ids_bytes + (size_t)need * H * sizeof(uint16_t);
+    p->h_stage.resize((bytes + 1) / 2);
+    char* base = reinterpret_cast<char*>(p->h_stage.data());
+    std::memcpy(base, taken.data(), need * sizeof(int32_t));
+    uint16_t* rows = reinterpret_cast<uint16_t*>(base + ids_bytes);
+    int64_t r = 0;
+    for (int s = 0; s < S; ++s) {
+      if (!present[s]) continue;
+      const uint16_t* A = static_cast<const uint16_t*>(A_host[s]);
+      const uint16_t* B = static_cast<const uint16_t*>(B_host[s]);
+      for (int j = 0; j < rank; ++j, ++r)        // column j of A (H x rank, row-major)
+        for (int64_t k = 0; k < H; ++k) rows[r * H + k] = A[k * rank + j];
+      for (int j = 0; j < rank; ++j, ++r)        // row j of B (rank x H, row-major)
+        std::memcpy(rows + r * H, B + (int64_t)j * H, H * sizeof(uint16_t));
+    }
+    cudaError_t e = cudaSuccess;
+    if (bytes > p->d_stage_bytes) {
+      if (p->d_stage) cudaFree(p->d_stage);
+      p->d_stage = nullptr;
+      p->d_stage_bytes = 0;
+      e = cudaMalloc(&p->d_stage, bytes);
+      if (e == cudaSuccess) p->d_stage_bytes = bytes;
+    }
+    std::vector<int32_t> dtab((size_t)S * kTabStride, -1);
+    for (int s = 0; s < S; ++s)
+      for (int half = 0; half < 2; ++half)
+        for (int j = 0; j < rank; ++j) dtab[(size_t)s * kTabStride + half * LORA_MAX_RANK + j] = table[((size_t)s * 2 + half) * rank + j];
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_stage, base, bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) {
+      ProfScope prof(p, LORA_KIND_SCATTER, st);
+      int rc = launch_scatter_pages(nullptr, static_cast<const int32_t*>(p->d_stage), need, p->H, p->pool_dev, st);
+      if (rc != LORA_OK) e = cudaErrorLaunchFailure;
+    }
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(p->d_ptab + (size_t)aid * S * kTabStride, dtab.data(), dtab.size() * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_rank + aid, &rank, sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+      rollback();
+      return lora_cuda_fail(e, "lora_adapter_load");
+    }
+  }
+  for (int32_t pg : taken) p->page_state[pg] = 2;
+  p->rank[aid] = rank;
+  p->tables[aid] = table;
+  p->adapter_pages += need;
+  p->resident += 1;
+  if (table_out) std::memcpy(table_out, table.data(), table.size() * sizeof(int32_t));
+  return LORA_OK;
+}
+
+int lora_adapter_unload(lora_pool* p, int32_t aid, lora_stream_t stream) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_unload: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
+    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_unload: adapter " + std::to_string(aid) + " is not loaded");
+  if (!p->planning) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(p->d_ptab + (size_t)aid * p->n_slots * kTabStride, 0xFF,
+                                    (size_t)p->n_slots * kTabStride * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->d_rank + aid, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return lora_cuda_fail(e, "lora_adapter_unload");
+  }
+  int64_t n = 0;
+  for (int32_t pg : p->tables[aid]) {
+    if (pg < 0) continue;
+    p->page_state[pg] = 0;
+    p->free_list.push_back(pg);
+    ++n;
+  }
+  p->adapter_pages -= n;
+  p->rank[aid] = 0;
+  p->tables[aid].clear();
+  p->resident -= 1;
+  return LORA_OK;
+}
+
+void lora_pool_stats(const lora_pool* p, lora_pool_stats_t* out) {
+  if (!p || !out) return;
+  out->num_pages = p->num_pages;
+  out->free_pages = (int64_t)p->free_list.size();
+  out->adapter_pages = p->adapter_pages;
+  out->reserved_pages = p->reserved_pages;
+  out->resident_adapters = p->resident;
+  out->max_adapters = p->max_adapters;
+}
+
+int lora_status(lora_pool* p, lora_stream_t stream) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_status: pool is NULL");
+  if (p->planning) return LORA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t h[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyAsync(h, p->d_err, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->d_err, 0, sizeof(h), st);
+  if (e != cudaSuccess) return lora_cuda_fail(e, "lora_status");
+  if (h[0] == 0) return LORA_OK;
+  std::string msg = "device check failed:";
+  if (h[1] & LORA_DEV_UNKNOWN_ADAPTER) msg += " unknown adapter id in token_adapter;";
+  if (h[1] & LORA_DEV_BAD_PAGE) msg += " page id out of range;";
+  if (h[1] & LORA_DEV_BAD_RANK) msg += " rank out of range;";
+  if (h[1] & LORA_DEV_WAIT_TIMEOUT) msg += " a bounded wait ran out;";
+  if (h[1] & LORA_DEV_BAD_SEGMENT) msg += " inconsistent segment list;";
+  return lora_fail(LORA_EDEVICE, msg);
+}
+
+// ---- segment workspace -----------------------------------------------------------------
+namespace {
+struct SegLayout {
+  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, shrink_work, n_shrink, expand_work, n_expand, s, delta, total;
+  int32_t max_seg, shrink_cap, expand_cap;
+};
+SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
+  SegLayout L{};
+  L.max_seg = std::min<int32_t>(T_max, p->max_adapters);
+  L.expand_cap = T_max / kExpandTokBlock + L.max_seg + 1;
+  L.shrink_cap = (T_max / kShrinkTokBlock + L.max_seg + 1) * (LORA_MAX_RANK / kShrinkRankGroup);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  L.perm = take((size_t)T_max * 4);
+  L.seg_off = take((size_t)(L.max_seg + 2) * 4);
+  L.seg_adapter = take((size_t)(L.max_seg + 1) * 4);
+  L.n_seg = take(16);
+  L.tok_adapter = take((size_t)T_max * 4);
+  L.shrink_work = take((size_t)L.shrink_cap * 16);
+  L.n_shrink = take(16);
+  L.expand_work = take((size_t)L.expand_cap * 8);
+  L.n_expand = take(16);
+  L.s = take((size_t)T_max * LORA_MAX_RANK * 4);
+  L.delta = take((size_t)T_max * p->H * 4);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+int64_t lora_segments_size(const lora_pool* p, int32_t T_max) {
+  if (!p || T_max < 1 || T_max > LORA_MAX_TOKENS) return (int64_t)lora_fail(LORA_EINVAL, "lora_segments_size: bad arguments");
+  return (int64_t)seg_layout(p, T_max).total;
+}
+
+int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T_max, lora_segments* seg) {
+  if (!p || !ws || !seg || T_max < 1 || T_max > LORA_MAX_TOKENS)
+    return lora_fail(LORA_EINVAL, "lora_segments_init: bad arguments");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return lora_fail(LORA_EINVAL, "lora_segments_init: workspace must be 256-byte aligned");
+  const SegLayout L = seg_layout(p, T_max);
+  if (ws_bytes < (int64_t)L.total)
+    return lora_fail(LORA_EINVAL, "lora_segments_init: workspace has " + std::to_string(ws_bytes) + " bytes, needs " +
+                                      std::to_string(L.total));
+  char* b = static_cast<char*>(ws);
+  seg->T_max = T_max;
+  seg->T = -1;
+  seg->max_seg = L.max_seg;
+  seg->H = p->H;
+  seg->perm = reinterpret_cast<int32_t*>(b + L.perm);
+  seg->seg_off = reinterpret_cast<int32_t*>(b + L.seg_off);
+  seg->seg_adapter = reinterpret_cast<int32_t*>(b + L.seg_adapter);
+  seg->n_seg = reinterpret_cast<int32_t*>(b + L.n_seg);
+  seg->tok_adapter = reinterpret_cast<int32_t*>(b + L.tok_adapter);
+  seg->shrink_work = reinterpret_cast<int32_t*>(b + L.shrink_work);
+  seg->n_shrink = reinterpret_cast<int32_t*>(b + L.n_shrink);
+  seg->expand_work = reinterpret_cast<int32_t*>(b + L.expand_work);
+  seg->n_expand = reinterpret_cast<int32_t*>(b + L.n_expand);
+  seg->shrink_cap = L.shrink_cap;
+  seg->expand_cap = L.expand_cap;
+  seg->s = reinterpret_cast<float*>(b + L.s);
+  seg->delta = reinterpret_cast<float*>(b + L.delta);
+  return LORA_OK;
+}
+
+}  // extern "C"

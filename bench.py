@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Benchmark: tokens/s through the batched multi-LoRA projections, and roofline fraction.
+
+One step = one pass of the whole hot path over one batch: the segment build (tokens grouped
+by adapter) plus lora_linear_forward on every projection slot of the workload (paged shrink,
+paged expand, tcgen05 base GEMM with the fused delta epilogue).  Adapters are resident
+(loading is set-up, not timed).  Default workload: the decode batch (H=4096, q/k/v/o,
+256 requests x 1 token, 64 adapters of rank 8..64, Zipf(1.0) request->adapter, pool of
+2^18 pages half filled with KV pages).  Other workloads with --config 1..5.
+
+Timing (our arm): the steps are captured into CUDA graphs with a 256 MB L2 flush between
+steps and CUDA events around every step and every kernel (events inside the graph, so host
+launch latency is excluded); steps are replayed in chunks; W untimed warm-up steps first.
+`value` = tokens x steps / summed step time (max over ranks).  `e2e` = the same metric
+through the public API with pinned host buffers: per step the H2D copy of the token ids and
+activations, the library calls, and the D2H copy of every slot's output.
+
+--impl reference times the CPU oracle (fp64, the definition of the layer) on a bounded
+sample of the same workload; there is no other reference implementation of this path.
+Multi-GPU (torchrun): every rank runs its own replica of the batch (independent problems,
+no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+GRAPH_CHUNK = 32
+
+
+# ------------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, use_cuda):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: str):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9 or not (t0 <= ts <= t1):
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_digest(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel_file, config_key):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        entry = json.load(open(path))[f"{os.path.basename(kernel_file)}:config{config_key}"]
+    except (KeyError, ValueError):
+        return None
+    if entry.get("source_sha") != source_digest(kernel_file):
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------- workload bytes / flops
+def algorithmic(wl):
+    """Algorithmic bytes and flops of one step (every slot), and of one base-GEMM launch."""
+    H, T, S = wl.H, wl.T, wl.n_slots
+    used = np.unique(wl.token_adapter[wl.token_adapter >= 0])
+    lora_pages = int(2 * wl.ranks[used].astype(np.int64).sum()) * S            # A and B, once per slot
+    sum_r = int(wl.ranks[wl.token_adapter[wl.token_adapter >= 0]].astype(np.int64).sum())
+    step_bytes = S * H * H * 2 + wl.n_inputs * T * H * 2 + S * T * H * 2 + lora_pages * H * 2
+    step_flops = S * (2 * T * H * H + 4 * H * sum_r)
+    gemm_bytes = H * H * 2 + 2 * T * H * 2
+    gemm_flops = 2 * T * H * H
+    return dict(step_bytes=step_bytes, step_flops=step_flops, gemm_bytes=gemm_bytes, gemm_flops=gemm_flops,
+                lora_page_bytes=lora_pages * H * 2, distinct_adapters=int(used.size), sum_rank=sum_r)
+
+
+# ------------------------------------------------------------------------------- our arm
+class Harness:
+    def __init__(self, key, device):
+        import torch
+        import adapter_gemm_lora_gb300 as L
+        from adapter_gemm_lora_gb300 import build as B
+        B.build()
+        self.L, self.torch = L, torch
+        self.wl = wl = workloads.make(key)
+        self.key = key
+        H, S, T = wl.H, wl.n_slots, wl.T
+        self.dev = device
+        to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(device).view(torch.bfloat16)  # noqa
+        self.pool_t = torch.full((wl.spec.pool_pages, H), float("nan"), dtype=torch.bfloat16, device=device)
+        self.pool = L.lora_pool_create(self.pool_t, wl.spec.pool_pages, H, S, wl.spec.n_adapters, wl.page_order)
+        L.lora_pool_reserve(self.pool, wl.kv_pages)
+        for a in range(wl.spec.n_adapters):
+            r = int(wl.ranks[a])
+            L.lora_adapter_load(self.pool, a, r, [wl.A(a, s) for s in range(S)], [wl.B(a, s) for s in range(S)], S)
+        self.x = [to_dev(wl.x(i)) for i in range(wl.n_inputs)]
+        self.W = [to_dev(wl.W(s)) for s in range(S)]
+        self.y = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(S)]
+        self.ta = torch.from_numpy(wl.token_adapter).to(device)
+        nbytes = L.lora_segments_size(self.pool, T)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.seg = L.lora_segments_init(self.pool, self.ws, nbytes, T)
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+    def step(self, stream):
+        L, wl = self.L, self.wl
+        L.lora_segments_build(self.pool, self.ta, wl.T, self.seg, stream=stream)
+        for s in range(wl.n_slots):
+            L.lora_linear_forward(self.pool, self.seg, s, self.x[wl.slot_input(s)], self.W[s], self.y[s], None,
+                                  stream=stream)
+
+    def capture(self, n_steps, stream):
+        """A graph of n_steps steps, each preceded by an L2 flush and bracketed by events."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(n_steps)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for i in range(n_steps):
+                self.flush_buf.zero_()
+                evs[i][0].record()
+                self.step(torch.cuda.current_stream().cuda_stream)
+                evs[i][1].record()
+        return g, evs
+
+    def run_timed(self, steps, warmup, dist):
+        torch, L = self.torch, self.L
+        stream = torch.cuda.Stream(device=self.dev)
+        with torch.cuda.stream(stream):
+            for _ in range(max(warmup, 1)):                 # eager warm-up (also sets kernel attributes)
+                self.flush_buf.zero_()
+                self.step(stream.cuda_stream)
+        torch.cuda.synchronize()
+        L.lora_profile_read(self.pool, reset=True)
+        L.lora_profile_enable(self.pool, True)
+        chunk = min(GRAPH_CHUNK, steps)
+        g_full, ev_full = self.capture(chunk, stream)          # kernels bracketed by profile events
+        counts = L.lora_profile_read(self.pool, reset=False)   # launches made during the capture
+        launches_per_graph = {k: v["launches"] for k, v in counts.items()}
+        L.lora_profile_enable(self.pool, False)
+        rem = steps % chunk
+        g_rem, ev_rem = self.capture(rem, stream) if rem else (None, [])
+        torch.cuda.synchronize()
+        for _ in range(max(1, warmup // chunk)):          # graph warm-up
+            g_full.replay()
+        torch.cuda.synchronize()
+        self.soak(g_full, 1.0)
+        n_full = steps // chunk
+        step_ms, kern_ms = [], {k: 0.0 for k in L.KINDS}
+        full_sets, rem_sets = 0, 0
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for _ in range(n_full):
+            g_full.replay()
+            torch.cuda.synchronize()
+            step_ms += [a.elapsed_time(b) for a, b in ev_full]
+            full_sets += 1
+            self._acc_kernels(kern_ms, rem_only=False)
+        if g_rem is not None:
+            g_rem.replay()
+            torch.cuda.synchronize()
+            step_ms += [a.elapsed_time(b) for a, b in ev_rem]
+            rem_sets += 1
+        torch.cuda.synchronize()
+        barrier(dist)
+        t1 = time.time()
+        assert len(step_ms) == steps
+        L.lora_status(self.pool, stream=stream.cuda_stream)
+        per_step = {k: launches_per_graph[k] // chunk for k in L.KINDS}
+        launches = {k: per_step[k] * steps for k in L.KINDS}
+        return dict(step_ms=step_ms, kern_ms=kern_ms, kern_sets=full_sets, launches=launches,
+                    launches_per_graph=launches_per_graph, launches_per_step=per_step, t0=t0, t1=t1)
+
+    def _acc_kernels(self, kern_ms, rem_only):
+        # the profile records are the events captured into the full-chunk graph, re-recorded by each replay
+        rec = self.L.lora_profile_read(self.pool, reset=False)
+        for k, v in rec.items():
+            kern_ms[k] += v["ms"]
+
+    def soak(self, graph, seconds):
+        """Untimed replays right before the timed region so the clock sampler sees the loaded GPU."""
+        end = time.time() + seconds
+        while time.time() < end:
+            graph.replay()
+            self.torch.cuda.synchronize()
+
+    def run_e2e(self, steps):
+        """Public-API path with pinned host buffers, copies inside the timed region."""
+        torch, L, wl = self.torch, self.L, self.wl
+        H, T, S = wl.H, wl.T, wl.n_slots
+        stream = torch.cuda.Stream(device=self.dev)
+        h_ta = torch.from_numpy(wl.token_adapter.copy()).pin_memory()
+        h_x = [torch.from_numpy(np.ascontiguousarray(wl.x(i)).view(np.int16)).view(torch.bfloat16).pin_memory()
+               for i in range(wl.n_inputs)]
+        h_y = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(S)]
+        d_ta = torch.empty_like(self.ta)
+        d_x = [torch.empty((T, H), dtype=torch.bfloat16, device=self.dev) for _ in range(wl.n_inputs)]
+        times = []
+        with torch.cuda.stream(stream):
+            for it in range(steps + 2):
+                self.flush_buf.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                d_ta.copy_(h_ta, non_blocking=True)
+                for i in range(wl.n_inputs):
+                    d_x[i].copy_(h_x[i], non_blocking=True)
+                L.lora_segments_build(self.pool, d_ta, T, self.seg, stream=stream.cuda_stream)
+                for s in range(S):
+                    L.lora_linear_forward(self.pool, self.seg, s, d_x[wl.slot_input(s)], self.W[s], self.y[s], None,
+                                          stream=stream.cuda_stream)
+                    h_y[s].copy_(self.y[s], non_blocking=True)
+                e1.record()
+                e1.synchronize()
+                if it >= 2:
+                    times.append(e0.elapsed_time(e1))
+        h2d = T * 4 + wl.n_inputs * T * H * 2
+        d2h = S * T * H * 2
+        return times, h2d, d2h
+
+
+def default_steps(key):
+    return {1: 2000, 2: 8000, 3: 400, 4: 2000, 5: 40}[key]
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, True)
+    device = torch.device("cuda", local)
+    key = args.config
+    steps = args.steps if args.steps is not None else default_steps(key)
+    h = Harness(key, device)
+    wl = h.wl
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = visible.split(",")[local] if visible else str(local)
+    clocks = ClockSampler(smi_index).start()
+    res = h.run_timed(steps, args.warmup, dist)
+    clocks.stop()
+    e2e_times, h2d, d2h = h.run_e2e(min(steps, 200 if key != 5 else 10))
+    total_ms = sum(res["step_ms"])
+    total_ms_max = max_over_ranks(total_ms, dist, device)
+    T = wl.T
+    value = world * T * steps / (total_ms_max / 1e3)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), dist, device)
+    peaks = load_peaks()
+    alg = algorithmic(wl)
+    ms_per_step = total_ms_max / steps
+    n_gemm = res["launches"]["gemm"]
+    gemm_ms = res["kern_ms"]["gemm"] / max(1, res["kern_sets"] * res["launches_per_graph"]["gemm"])
+    shares = {k: v / max(1e-12, sum(res["kern_ms"].values())) for k, v in res["kern_ms"].items()}
+    # dominant kernel: the base GEMM; its roof follows the workload's arithmetic intensity
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    gemm_ai = alg["gemm_flops"] / alg["gemm_bytes"]
+    kernel_file = os.path.join(ROOT, "adapter_gemm_lora_gb300", "csrc", "gemm_tcgen05.cu")
+    traffic = committed_traffic(kernel_file, key)
+    if gemm_ai < ridge:
+        achieved = alg["gemm_bytes"] / (gemm_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic}
+    else:
+        achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+        pk = peaks["bf16_tflops_sustained"] if key == 5 else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(achieved / pk, 4), "traffic": traffic}
+    roof.update({"kernel": "gemm_lora_kernel", "peak_source": peaks["source"], "avg_launch_us": round(gemm_ms * 1e3, 2),
+                 "algorithmic_per_launch": alg["gemm_bytes"] if roof["bound"] == "hbm" else alg["gemm_flops"]})
+    step_s = ms_per_step / 1e3
+    t_hbm = alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg["step_flops"] / (peaks["bf16_tflops"] * 1e12)
+    step_roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_us": round(max(t_hbm, t_tc) * 1e6, 2),
+                 "measured_us": round(step_s * 1e6, 2), "frac": round(max(t_hbm, t_tc) / step_s, 4),
+                 "algorithmic_bytes": alg["step_bytes"], "algorithmic_flops": alg["step_flops"],
+                 "achieved_gbs": round(alg["step_bytes"] / step_s / 1e9, 1),
+                 "achieved_tflops": round(alg["step_flops"] / step_s / 1e12, 1)}
+    line = {
+        "metric": "tokens/s through batched multi-LoRA projections",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights and adapters)",
+        "config": {"workload": wl.spec.name, "description": wl.spec.description, "H": wl.H, "T": T,
+                   "slots": wl.n_slots, "adapters_resident": wl.spec.n_adapters,
+                   "distinct_adapters_in_batch": alg["distinct_adapters"], "pool_pages": wl.spec.pool_pages,
+                   "parallelism": f"replicas x{world}", "l2": "flushed (256 MB write) before every step",
+                   "timing": "CUDA graph replay, events per step and per kernel inside the graph"},
+        "roofline": roof,
+        "step_roofline": step_roof,
+        "kernel_share": {k: round(v, 4) for k, v in shares.items() if res["kern_ms"][k] > 0},
+        "gpu_launches": int(sum(res["launches"].values())),
+        "gpu_launches_per_step": res["launches_per_step"],
+        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "path": "eager public API calls, pinned host buffers"},
+        "clocks": clocks.summary(res["t0"] - 1.5, res["t1"]),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------- oracle (CPU)
+def oracle_scene(wl, slots, tokens):
+    """The oracle's pool for the given slots (its own bookkeeping and placement)."""
+    import oracle as O
+
+    class Sparse(dict):
+        def __setitem__(self, k, v):
+            super().__setitem__(int(k), np.asarray(v, np.uint16).copy())
+
+        def __getitem__(self, idx):
+            idx = np.asarray(idx)
+            return np.stack([dict.__getitem__(self, int(i)) for i in idx.reshape(-1)]).reshape(idx.shape + (wl.H,))
+
+    model = O.PoolModel(wl.spec.pool_pages, wl.n_slots, wl.spec.n_adapters, wl.page_order)
+    model.reserve(wl.kv_pages)
+    pool = Sparse()
+    used = set(int(a) for a in wl.token_adapter[tokens] if a >= 0)
+    for a in range(wl.spec.n_adapters):
+        _, tab = model.load(a, int(wl.ranks[a]), [True] * wl.n_slots)
+        if a in used:
+            O.place_adapter(pool, tab, [wl.A(a, s) if s in slots else None for s in range(wl.n_slots)],
+                            [wl.B(a, s) if s in slots else None for s in range(wl.n_slots)])
+    return model, pool
+
+
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_sample(wl, seconds):
+    """Tokens and slots of a bounded oracle sample: every slot for small stacks, else 4 slots."""
+    rng = np.random.default_rng(1234)
+    slots = list(range(wl.n_slots)) if wl.n_slots <= 4 else [0, 1, 2, 3]
+    n_tok = min(wl.T, 64)
+    tokens = np.sort(rng.choice(wl.T, size=n_tok, replace=False))
+    return slots, tokens
+
+
+def cpu_baseline(wl, seconds=15.0):
+    slots, tokens = oracle_sample(wl, seconds)
+    model, pool = oracle_scene(wl, set(slots), tokens)
+    xs = {i: wl.x(i) for i in {wl.slot_input(s) for s in slots}}
+    Ws = {s: wl.W(s) for s in slots}
+    import oracle as O
+    t0 = time.time()
+    reps = 0
+    while True:
+        for s in slots:
+            O.linear_forward(pool, model.tables, wl.token_adapter, s, xs[wl.slot_input(s)], Ws[s], tokens=tokens)
+        reps += 1
+        if time.time() - t0 >= seconds or reps >= 1000:
+            break
+    el = time.time() - t0
+    # tokens through the whole stack per second: each sampled token passed len(slots) of n_slots slots
+    value = reps * len(tokens) * (len(slots) / wl.n_slots) / el
+    return {"value": round(value, 3), "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"{len(tokens)} of {wl.T} tokens through {len(slots)} of {wl.n_slots} slots, "
+                      f"repeated {reps}x over {el:.1f} s (fp64 NumPy, per-token page-table gathers)"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    key = args.config
+    wl = workloads.make(key)
+    steps = args.steps if args.steps is not None else 10
+    per_step = max(0.5, min(6.0, 150.0 / max(1, steps + args.warmup)))
+    slots, tokens = oracle_sample(wl, per_step)
+    model, pool = oracle_scene(wl, set(slots), tokens)
+    xs = {i: wl.x(i) for i in {wl.slot_input(s) for s in slots}}
+    Ws = {s: wl.W(s) for s in slots}
+    import oracle as O
+
+    def one():
+        for s in slots:
+            O.linear_forward(pool, model.tables, wl.token_adapter, s, xs[wl.slot_input(s)], Ws[s], tokens=tokens)
+    for _ in range(args.warmup):
+        one()
+    times = []
+    for _ in range(steps):
+        t0 = time.time()
+        one()
+        times.append(time.time() - t0)
+    tot = sum(times)
+    value = steps * len(tokens) * (len(slots) / wl.n_slots) / tot
+    line = {"impl": "reference", "metric": "tokens/s through batched multi-LoRA projections", "value": round(value, 3),
+            "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.spec.name, "description": wl.spec.description, "H": wl.H, "T": wl.T,
+                       "slots": wl.n_slots},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+                             "sample": f"{len(tokens)} of {wl.T} tokens through {len(slots)} of {wl.n_slots} "
+                                       f"slots per step"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+/*
+ * lora.h - C boundary of the GB300 multi-adapter LoRA projection library (liblora.so).
+ *
+ * What it computes ("S-LoRA, in depth", section "Merge or keep adapters separate"):
+ * for a batch of T tokens, each carrying its own adapter id a(t), one projection
+ * slot computes
+ *
+ *     y_t = x_t W + (x_t A_{a(t)}) B_{a(t)}          (unmerged LoRA)
+ *
+ * with W shared by every token (H x H) and the low-rank factors A (H x r),
+ * B (r x H) of the token's own adapter, r in [1, 64].  A token with adapter id -1
+ * gets y_t = x_t W.  The factors live in a unified page pool (same page, section
+ * "Unified paging: adapters and KV cache in one pool"): the pool is an array of
+ * pages, one page holds one vector of H values, a rank-r A or B takes r pages, and
+ * adapter pages come from the same free list as KV-cache pages.
+ *
+ * Conventions for every entry point
+ *  - Pointers named *_host are host memory; every other data pointer is device memory
+ *    on the current CUDA device.  Device memory for x, W, y, the pool storage and the
+ *    segment workspace is owned by the caller (e.g. PyTorch tensors); the library keeps
+ *    non-owning pointers and never frees them.
+ *  - Element types: bf16 for pool pages, x, W, y and the host A/B factors (raw 16-bit
+ *    patterns); fp32 for the optional LoRA delta; int32 for token adapter ids.
+ *  - Device work is enqueued on the caller's stream (a cudaStream_t passed as
+ *    lora_stream_t; NULL = the legacy default stream).  Only lora_adapter_load and
+ *    lora_status synchronise that stream.
+ *  - Return value: LORA_OK (0) or a negative LORA_E* code; lora_last_error() then gives
+ *    a message for the calling thread.  A failing call leaves the pool as it was.
+ *  - Adapters are immutable once loaded; there is no global "active adapter": the
+ *    adapter of every token travels in each call ("Switch Adapters by Routing Requests
+ *    Through Resident, Verified State": request-scoped binding; an unknown adapter is
+ *    an error).
+ *  - One pool may be used from one host thread at a time.
+ */
+#ifndef ADAPTER_GEMM_LORA_H
+#define ADAPTER_GEMM_LORA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lora_stream_t;  /* identical to cudaStream_t */
+
+#define LORA_OK                0
+#define LORA_EINVAL           -1   /* null pointer, bad size, H % 64 != 0, slot or id out of range */
+#define LORA_ENOPAGES         -2   /* the free list holds fewer pages than asked for */
+#define LORA_EUNKNOWN_ADAPTER -3   /* adapter id not loaded */
+#define LORA_ERANK            -4   /* rank outside [1, LORA_MAX_RANK] */
+#define LORA_EEXIST           -5   /* adapter id already loaded */
+#define LORA_ECUDA            -6   /* a CUDA runtime or driver call failed */
+#define LORA_EDEVICE          -7   /* a device-side check failed (see lora_status) */
+
+#define LORA_MAX_RANK      64
+#define LORA_MAX_ADAPTERS  16384    /* adapter ids are indices in [0, max_adapters) */
+#define LORA_MAX_TOKENS    65536    /* tokens per batch */
+
+typedef struct lora_pool lora_pool;
+
+typedef struct lora_pool_stats_t {
+  int64_t num_pages;
+  int64_t free_pages;
+  int64_t adapter_pages;
+  int64_t reserved_pages;      /* KV / filler pages taken by lora_pool_reserve */
+  int32_t resident_adapters;
+  int32_t max_adapters;
+} lora_pool_stats_t;
+
+/*
+ * Per-batch token grouping, built on the device by lora_segments_build and read by
+ * lora_linear_forward.  Set up with lora_segments_init over a caller-allocated device
+ * workspace of lora_segments_size() bytes; every pointer below points into it.
+ * Device arrays (after a build with T tokens, S = *n_seg segments):
+ *   perm[T]          token indices, stable-sorted by adapter id; id -1 tokens first;
+ *   seg_off[S + 1]   segment s covers perm[seg_off[s] .. seg_off[s+1]); seg_off[0] is
+ *                    the number of no-adapter tokens and seg_off[S] = T;
+ *   seg_adapter[S]   adapter id of segment s, ascending;
+ *   n_seg[1]         S;
+ * plus work lists and fp32 scratch (the shrink output s and the LoRA delta) used by
+ * lora_linear_forward.  Calls that use the same workspace must be ordered on one
+ * stream: the scratch is reused by every projection slot.
+ */
+typedef struct lora_segments {
+  int32_t T_max;          /* token capacity of the workspace */
+  int32_t T;              /* tokens of the last build (host copy), -1 before any build */
+  int32_t max_seg;        /* capacity of the segment arrays */
+  int32_t H;              /* hidden size of the pool the workspace was sized for */
+  int32_t* perm;
+  int32_t* seg_off;
+  int32_t* seg_adapter;
+  int32_t* n_seg;
+  int32_t* tok_adapter;   /* [T_max] validated adapter id per token (-1 = none or rejected) */
+  int32_t* shrink_work;   /* [4 * shrink_cap] (segment, token block, rank group, -) */
+  int32_t* n_shrink;
+  int32_t* expand_work;   /* [2 * expand_cap] (segment, token block) */
+  int32_t* n_expand;
+  int32_t shrink_cap;
+  int32_t expand_cap;
+  float*   s;             /* [T_max][64] x_t A for the token's adapter (fp32) */
+  float*   delta;         /* [T_max][H]  (x_t A) B (fp32) */
+} lora_segments;
+
+/*
+ * Create a pool over caller-owned device storage.
+ *   pool_dev         device bf16 [num_pages][H]; NULL creates a planning pool that only
+ *                    does the page bookkeeping (no device memory, no copies, no kernels);
+ *   num_pages        1 .. 2^31-1;   H: multiple of 64, 64 .. 16384;
+ *   n_slots          projection slots (e.g. 4 per layer for q, k, v, o), >= 1;
+ *   max_adapters     adapter ids must lie in [0, max_adapters), 1 .. LORA_MAX_ADAPTERS;
+ *   page_order_host  nullable int64 [num_pages]: the initial free list (a permutation of
+ *                    0..num_pages-1); pages are taken from its END, as the pool sketch in
+ *                    "Unified paging" pops its free list.  NULL = 0, 1, ..., num_pages-1.
+ * The library allocates its own device page tables (max_adapters * n_slots * 512 bytes)
+ * and an error word.  *out receives the handle; free it with lora_pool_destroy.
+ */
+int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slots,
+                     int32_t max_adapters, const int64_t* page_order_host, lora_pool** out);
+
+/* Take n pages from the free list for KV cache or other non-adapter use (the sketch's
+ * grow_kv).  page_ids_host (int64 [n], out) receives them in the order taken.
+ * LORA_ENOPAGES if fewer than n are free (nothing taken). */
+int lora_pool_reserve(lora_pool* pool, int64_t n, int64_t* page_ids_host);
+
+/* Give back n reserved pages (appended to the free list in the order given).
+ * LORA_EINVAL if any id is not currently reserved or appears twice (nothing released). */
+int lora_pool_release(lora_pool* pool, int64_t n, const int64_t* page_ids_host);
+
+/*
+ * Load an adapter ("Unified paging" sketch, ensure_adapter): take 2 * rank pages per slot
+ * that carries LoRA and copy the factors into them.
+ *   A_host[slot]   host bf16 [H][rank] row-major, or NULL: no LoRA on that slot;
+ *   B_host[slot]   host bf16 [rank][H] row-major (ignored where A_host[slot] is NULL);
+ *   page_table_host (out, nullable) int32 [n_slots][2][rank]: [slot][0][j] = page holding
+ *                  column j of A, [slot][1][j] = page holding row j of B, -1 for a slot
+ *                  without LoRA.  Pages are taken in that order (slot, A then B, j).
+ * In a planning pool A_host may be NULL (every slot carries LoRA) and no data is read.
+ * Synchronises `stream` (the host staging buffer is reused).
+ * Errors: LORA_EINVAL (id range, null B where A is set), LORA_ERANK, LORA_EEXIST,
+ * LORA_ENOPAGES (pool unchanged), LORA_ECUDA.
+ */
+int lora_adapter_load(lora_pool* pool, int32_t adapter_id, int32_t rank,
+                      const void* const* A_host, const void* const* B_host,
+                      lora_stream_t stream, int32_t* page_table_host);
+
+/* Return an adapter's pages to the free list and clear its device page table (enqueued on
+ * `stream`; work already enqueued before it on that stream still sees the adapter).
+ * LORA_EUNKNOWN_ADAPTER if it is not loaded. */
+int lora_adapter_unload(lora_pool* pool, int32_t adapter_id, lora_stream_t stream);
+
+/* Device workspace bytes lora_segments_init needs for batches of up to T_max tokens
+ * (dominated by the fp32 delta, T_max * H * 4 bytes).  Returns < 0 on bad arguments. */
+int64_t lora_segments_size(const lora_pool* pool, int32_t T_max);
+
+/* Carve `workspace_dev` (>= lora_segments_size bytes, 256-byte aligned) into *seg. */
+int lora_segments_init(const lora_pool* pool, void* workspace_dev, int64_t workspace_bytes,
+                       int32_t T_max, lora_segments* seg);
+
+/*
+ * Group a batch's tokens by adapter (stable: ascending adapter id, ties by token index).
+ *   token_adapter  device int32 [T]: adapter id per token, -1 = no adapter;
+ *   T              0 .. seg->T_max.
+ * Ids that are not loaded are treated as "no adapter" and raise the device error word
+ * (LORA_EUNKNOWN_ADAPTER, reported by lora_status).  Built once per batch, reused by every
+ * slot's lora_linear_forward.
+ */
+int lora_segments_build(lora_pool* pool, const int32_t* token_adapter, int32_t T,
+                        lora_segments* seg, lora_stream_t stream);
+
+/*
+ * One projection slot over the batch last built into `seg`:
+ *     y[t, n] = bf16_rne( sum_k x[t,k] W[n,k]  +  sum_j s[t,j] B_{a(t)}[j, n] ),
+ *     s[t, j] = sum_k x[t,k] A_{a(t)}[k, j]        (fp32; bf16 inputs, fp32 accumulation)
+ *   x      device bf16 [T][H] row-major;
+ *   W      device bf16 [H][H] in nn.Linear layout W[out][in] (so y = x W^T);
+ *   y      device bf16 [T][H] row-major, written (out of place; must not alias x);
+ *   delta_dbg  nullable device fp32 [T][H]: receives the LoRA term alone (0 for tokens
+ *          without LoRA on this slot), for parity tests.
+ * Kernels: paged shrink (s), paged expand (delta), tcgen05 base GEMM with an epilogue that
+ * adds the delta before the single bf16 rounding.
+ * Errors: LORA_EINVAL (slot, pointers, no batch built), LORA_ECUDA (launch failure).
+ */
+int lora_linear_forward(lora_pool* pool, const lora_segments* seg, int32_t slot,
+                        const void* x, const void* W, void* y, float* delta_dbg,
+                        lora_stream_t stream);
+
+/* Synchronise `stream`, read and clear the device error word.  LORA_OK, or LORA_EDEVICE
+ * with lora_last_error() naming the failed check (unknown adapter id, page id out of
+ * range, bad rank, a bounded wait that ran out). */
+int lora_status(lora_pool* pool, lora_stream_t stream);
+
+/* Page accounting: free, adapter and reserved pages, resident adapters. */
+void lora_pool_stats(const lora_pool* pool, lora_pool_stats_t* out);
+
+/* Message for the last non-zero status returned on the calling thread ("" if none). */
+const char* lora_last_error(void);
+
+/*
+ * Kernel accounting for benchmarks.  Every kernel this library launches for `pool` is counted
+ * by kind: 0 segment build, 1 shrink, 2 expand, 3 base GEMM, 4 page scatter (adapter loads).
+ * With profiling enabled, each launch is also bracketed by CUDA events recorded on the
+ * stream it runs on (also inside a stream capture: the events then become graph nodes and
+ * are re-recorded by every replay).  lora_profile_read synchronises those events and
+ * writes, for kinds 0 .. n_kinds-1, the launch count and the summed device milliseconds
+ * (0 where profiling was off); with `reset` != 0 it then clears both records.
+ * Events cost ~1 us of host time per launch.
+ */
+#define LORA_KIND_SEGMENTS 0
+#define LORA_KIND_SHRINK   1
+#define LORA_KIND_EXPAND   2
+#define LORA_KIND_GEMM     3
+#define LORA_KIND_SCATTER  4
+#define LORA_N_KINDS       5
+int lora_profile_enable(lora_pool* pool, int32_t enable);
+int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, double* ms_host,
+                      int32_t reset);
+
+/* Free the pool's own host and device memory (not the caller's storage). NULL is ignored. */
+void lora_pool_destroy(lora_pool* pool);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAPTER_GEMM_LORA_H */

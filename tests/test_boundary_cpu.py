@@ -1,0 +1,193 @@
+"""The C boundary without a GPU: the library loads, exports every declared entry point, and
+its host page bookkeeping (planning pools) matches the oracle's pool model exactly."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from adapter_gemm_lora_gb300 import build
+    build.build()
+    import adapter_gemm_lora_gb300 as lib
+    lib.library()
+    return lib
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "lora.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert declared == sorted(L.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (lora_[a-z_]+)", out))
+    assert set(declared) <= exported, set(declared) - exported
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "lora.h"\nint main(void){lora_pool_stats_t s; (void)s; return LORA_OK;}\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", str(src),
+                        "-o", str(tmp_path / "t.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def _mirror_ops(L, num_pages, n_slots, max_adapters, order, ops):
+    """Apply the same operations to a planning pool and to the oracle's model; compare everything."""
+    pool = L.lora_pool_create(None, num_pages, 64, n_slots, max_adapters, order)
+    model = O.PoolModel(num_pages, n_slots, max_adapters, order)
+    try:
+        for op in ops:
+            kind = op[0]
+            if kind == "reserve":
+                st, ids = model.reserve(op[1])
+                try:
+                    got = L.lora_pool_reserve(pool, op[1])
+                    assert st == O.OK and got.tolist() == ids
+                except L.LoraError as e:
+                    assert e.code == st
+            elif kind == "release":
+                st = model.release(op[1])
+                try:
+                    L.lora_pool_release(pool, op[1])
+                    assert st == O.OK
+                except L.LoraError as e:
+                    assert e.code == st
+            elif kind == "load":
+                _, aid, rank, present = op
+                st, tab = model.load(aid, rank, present)
+                A = [np.zeros(1, np.uint16) if p else None for p in present]
+                try:
+                    got = L.lora_adapter_load(pool, aid, rank, A, None, n_slots, planning=True)
+                    assert st == O.OK, f"library loaded, oracle said {st}"
+                    assert np.array_equal(got.astype(np.int64), tab)
+                except L.LoraError as e:
+                    assert e.code == st, (e, st)
+            elif kind == "unload":
+                st = model.unload(op[1])
+                try:
+                    L.lora_adapter_unload(pool, op[1], planning=True)
+                    assert st == O.OK
+                except L.LoraError as e:
+                    assert e.code == st
+            s = L.lora_pool_stats(pool)
+            ms = model.stats()
+            assert (s["free"], s["adapter"], s["reserved"], s["resident_adapters"]) == \
+                (ms["free"], ms["adapter"], ms["reserved"], ms["resident_adapters"])
+    finally:
+        L.lora_pool_destroy(pool)
+
+
+def test_pool_matches_oracle_random_ops(L):
+    rng = np.random.default_rng(5)
+    n_slots, max_ad, num_pages = 3, 12, 500
+    ops, reserved = [], []
+    for _ in range(400):
+        k = rng.integers(0, 5)
+        if k == 0:
+            ops.append(("reserve", int(rng.integers(0, 40))))
+        elif k == 1 and ops:
+            ops.append(("release", [int(v) for v in rng.choice(num_pages, size=rng.integers(1, 4), replace=False)]))
+        elif k in (2, 3):
+            present = [bool(v) for v in rng.random(n_slots) < 0.8]
+            ops.append(("load", int(rng.integers(-1, max_ad + 1)), int(rng.integers(0, 66)), present))
+        else:
+            ops.append(("unload", int(rng.integers(-1, max_ad + 1))))
+    _mirror_ops(L, num_pages, n_slots, max_ad, rng.permutation(num_pages), ops)
+
+
+def test_release_exactly_reserved(L):
+    rng = np.random.default_rng(6)
+    order = rng.permutation(64)
+    pool = L.lora_pool_create(None, 64, 64, 1, 4, order)
+    model = O.PoolModel(64, 1, 4, order)
+    ids = L.lora_pool_reserve(pool, 10)
+    _, mids = model.reserve(10)
+    assert ids.tolist() == mids
+    with pytest.raises(L.LoraError) as e:
+        L.lora_pool_release(pool, [int(ids[0]), int(ids[0])])
+    assert e.value.code == L.LORA_EINVAL
+    L.lora_pool_release(pool, ids[::-1])
+    model.release(list(ids[::-1]))
+    t = L.lora_adapter_load(pool, 0, 7, None, None, 1, planning=True)
+    _, mt = model.load(0, 7, [True])
+    assert np.array_equal(t.astype(np.int64), mt)
+    L.lora_pool_destroy(pool)
+
+
+def test_enopages_at_boundary_leaves_pool_unchanged(L):
+    pool = L.lora_pool_create(None, 100, 64, 2, 8)
+    L.lora_pool_reserve(pool, 36)
+    L.lora_adapter_load(pool, 0, 16, None, None, 2, planning=True)        # 64 pages: exactly what is left
+    before = L.lora_pool_stats(pool)
+    with pytest.raises(L.LoraError) as e:
+        L.lora_adapter_load(pool, 1, 1, [np.zeros(1, np.uint16), None], None, 2, planning=True)
+    assert e.value.code == L.LORA_ENOPAGES
+    assert L.lora_pool_stats(pool) == before
+    with pytest.raises(L.LoraError) as e:
+        L.lora_pool_reserve(pool, 1)
+    assert e.value.code == L.LORA_ENOPAGES
+    L.lora_pool_destroy(pool)
+
+
+def test_worked_example_capacity_plan(L):
+    """A planning pool sized like the worked example: 2,000 rank-16 adapters on q/k/v/o over
+    32 layers take 2000 * 4096 pages of 4096 values (about 62 GiB at 2 bytes per value)."""
+    slots = 4 * 32
+    pool = L.lora_pool_create(None, 2000 * 4096, 4096, slots, 2000)
+    for a in range(2000):
+        L.lora_adapter_load(pool, a, 16, None, None, slots, planning=True)
+    s = L.lora_pool_stats(pool)
+    assert s["adapter"] == 2000 * O.PoolModel.pages_for_adapter(16, 32, 4) and s["free"] == 0
+    assert abs(s["adapter"] * 4096 * 2 / 2**30 - 62.5) < 1e-9
+    with pytest.raises(L.LoraError):
+        L.lora_adapter_load(pool, 1999, 16, None, None, slots, planning=True)   # already loaded
+    L.lora_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 0, 64, 1, 1), -1), ((None, 10, 63, 1, 1), -1), ((None, 10, 64, 0, 1), -1),
+    ((None, 10, 64, 1, 0), -1), ((None, 10, 64, 1, 16385), -1), ((None, 10, 32768, 1, 1), -1)])
+def test_pool_create_rejects_bad_geometry(L, args, code):
+    with pytest.raises(L.LoraError) as e:
+        L.lora_pool_create(*args)
+    assert e.value.code == code and e.value.message
+
+
+def test_page_order_must_be_permutation(L):
+    with pytest.raises(L.LoraError):
+        L.lora_pool_create(None, 4, 64, 1, 1, np.array([0, 1, 1, 3]))
+
+
+def test_workload_tables_match_oracle_config2(L):
+    """Placing config 2's 64 adapters after 50% KV filler gives the oracle's page tables."""
+    w = workloads.make(2)
+    pool = L.lora_pool_create(None, w.spec.pool_pages, w.H, w.n_slots, w.spec.n_adapters, w.page_order)
+    model = O.PoolModel(w.spec.pool_pages, w.n_slots, w.spec.n_adapters, w.page_order)
+    assert L.lora_pool_reserve(pool, w.kv_pages).tolist() == model.reserve(w.kv_pages)[1]
+    for a in range(w.spec.n_adapters):
+        t = L.lora_adapter_load(pool, a, int(w.ranks[a]), None, None, w.n_slots, planning=True)
+        assert np.array_equal(t.astype(np.int64), model.load(a, int(w.ranks[a]), [True] * w.n_slots)[1])
+    L.lora_pool_destroy(pool)
+
+
+def test_device_calls_rejected_on_planning_pool(L):
+    pool = L.lora_pool_create(None, 10, 64, 1, 1)
+    seg = L.lora_segments()
+    with pytest.raises(L.LoraError) as e:
+        L.lora_linear_forward(pool, seg, 0, 16, 16, 32, stream=0)
+    assert e.value.code == L.LORA_EINVAL
+    assert L.lora_segments_size(pool, 100) > 100 * 64 * 4
+    L.lora_pool_destroy(pool)
