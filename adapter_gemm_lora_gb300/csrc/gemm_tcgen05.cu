@@ -14,9 +14,15 @@
 // column = token.  That suits the epilogue: a warp covers 32 consecutive features of
 // one token, so delta loads and y stores are contiguous along the feature dimension.
 //
-// Per CTA: one 128 x BN output tile over the full K.  Warp 0 issues TMA loads into a
+// Per CTA: one 128 x BN output tile over a slice of K.  Warp 0 issues TMA loads into a
 // 4-stage ring, warp 1 owns TMEM and a single thread issues the MMAs, then all 8 warps
 // drain TMEM (warp w reads TMEM lanes 32*(w%4) .. +31, half the columns each).
+// Small grids (decode batches: H/128 x 1 tiles for 152 SMs) split K over the CTAs of a
+// thread-block cluster; each CTA then owns BN/ks token columns, receives the other CTAs'
+// fp32 partials for them through distributed shared memory, and sums them in split order
+// (deterministic) before the epilogue.  The mainloop reads only x and W, so the kernel is
+// launched as a programmatic dependent of the LoRA kernels before it and waits for them
+// (griddepcontrol.wait) only before its epilogue reads the delta.
 // Every mbarrier wait is bounded (~2 s); on expiry the CTA raises the device error word,
 // skips the rest of its work and frees TMEM before returning.
 #include <cuda.h>
@@ -48,7 +54,7 @@ struct GemmParams {
   const int32_t* tok_adapter;
   const int32_t* ptab;
   int32_t* err;
-  int32_t T, H, BN, n_kb, slot, n_slots;
+  int32_t T, H, BN, n_kb, ks, slot, n_slots;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -93,12 +99,44 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ---- TMA --------------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---- clusters and programmatic dependent launch --------------------------------------------
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 
 // ---- tcgen05 ----------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -178,8 +216,11 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES, bar_accum = bar_full + 16 * STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM;
-  const int t0 = blockIdx.y * p.BN;
+  const int split = blockIdx.x;                     // == rank in the (ks, 1, 1) cluster
+  const int m0 = blockIdx.y * BM;
+  const int t0 = blockIdx.z * p.BN;
+  const int kb0 = split * p.n_kb / p.ks, kb1 = (split + 1) * p.n_kb / p.ks;
+  const int nk = kb1 - kb0;
   const uint32_t ncols = tmem_cols_for(p.BN);
 
   if (threadIdx.x == 0) {
@@ -204,25 +245,28 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 0) {
     if (lane == 0) {                                  // TMA producer
       const uint32_t tx = A_BYTES + (uint32_t)p.BN * BK * 2;
-      for (int kb = 0; kb < p.n_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+      const uint64_t pol_w = policy_evict_first();    // W streams through once
+      const uint64_t pol_x = policy_evict_last();     // x is re-read by every feature tile
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
         }
         mbar_arrive_expect_tx(bar_full + 8 * s, tx);
-        tma_load_2d(s_base + s * STAGE_BYTES, &tm_w, kb * BK, m0, bar_full + 8 * s);
-        tma_load_2d(s_base + s * STAGE_BYTES + A_BYTES, &tm_x, kb * BK, t0, bar_full + 8 * s);
+        const int kc = (kb0 + i) * BK;
+        tma_load_2d(s_base + s * STAGE_BYTES, &tm_w, kc, m0, bar_full + 8 * s, pol_w);
+        tma_load_2d(s_base + s * STAGE_BYTES + A_BYTES, &tm_x, kc, t0, bar_full + 8 * s, pol_x);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {                                  // MMA issuer
       const uint32_t idesc = make_idesc_bf16(BM, p.BN);
-      for (int kb = 0; kb < p.n_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
         if (!mbar_wait(bar_full + 8 * s, ph)) {
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
@@ -232,7 +276,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const uint64_t bd = sw128_kmajor_desc(s_base + s * STAGE_BYTES + A_BYTES);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)             // 16-element K steps = 32 bytes = 2 descriptor units
-          mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
         mma_commit(bar_empty + 8 * s);
       }
       mma_commit(bar_accum);
@@ -241,18 +285,50 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   }
 
   // ---- epilogue: all 8 warps ----
-  const bool ok = mbar_wait(bar_accum, 0);
+  bool ok = mbar_wait(bar_accum, 0);
   if (!ok && lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
-  __syncwarp();
+  ok = __syncthreads_and(ok) != 0;
   tc_fence_after();
+  pdl_wait_then_release();         // the delta and validated ids come from the kernels before this one
+  const int q = warp & 3, h = warp >> 2;
+  const int row = q * 32 + lane;
+  const int n = m0 + row;
+  const int cols = p.BN / p.ks;     // token columns this CTA finishes
+  const uint32_t recv = s_base;     // [ks][cols][128] fp32 partials received from the cluster
+  const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+  if (p.ks > 1) {
+    cluster_sync_all();             // every CTA is past its mainloop: stage memory may be overwritten
+    if (ok) {
+      for (int c = h; c < p.BN / 32; c += 2) {
+        const int owner = (c * 32) / cols;
+        if (owner == split) continue;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
+        tmem_ld_wait();
+        const uint32_t base = recv + (uint32_t)(((split * cols + c * 32 - owner * cols) * BM + row) * 4);
+        const uint32_t remote = map_to_cta(base, (uint32_t)owner);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) st_cluster_f32(remote + (uint32_t)(i * BM * 4), __uint_as_float(v[i]));
+      }
+    }
+    cluster_sync_all();             // all partials delivered
+  }
   if (ok) {
-    const int q = warp & 3, h = warp >> 2;
-    const int n = m0 + q * 32 + lane;
-    const int n_chunks = p.BN / 32;
-    for (int c = h; c < n_chunks; c += 2) {
+    for (int cc = h; cc < cols / 32; cc += 2) {
+      const int c = split * (cols / 32) + cc;
       uint32_t v[32];
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+      tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
       tmem_ld_wait();
+      if (p.ks > 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float sum = 0.f;
+          for (int src = 0; src < p.ks; ++src)
+            sum += src == split ? __uint_as_float(v[i])
+                                : ld_shared_f32(recv + (uint32_t)(((src * cols + cc * 32 + i) * BM + row) * 4));
+          v[i] = __float_as_uint(sum);
+        }
+      }
       const int tc = t0 + c * 32;
       const int tl = tc + lane;
       int present = 0;
@@ -317,10 +393,16 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
     if (e != cudaSuccess) return lora_cuda_fail(e, "gemm_lora_kernel attribute");
     attr_set = true;
   }
+  const int n_sm = device_sm_count();
   const int n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
   int bn = (G.T + n_tiles - 1) / n_tiles;
   bn = ((bn + 31) / 32) * 32;
   if (bn > MAX_BN) bn = MAX_BN;
+  const int m_tiles = (G.H + BM - 1) / BM;
+  const int n_kb = G.H / BK;
+  // Split K over a cluster while the grid would leave most SMs idle.
+  int ks = 1;
+  while (ks < 8 && m_tiles * n_tiles * ks * 2 <= n_sm && n_kb / (ks * 2) >= 4 && bn % (32 * ks * 2) == 0) ks *= 2;
   CUtensorMap tm_w, tm_x;
   int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, BM);
   if (rc != LORA_OK) return rc;
@@ -335,11 +417,25 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.T = G.T;
   P.H = G.H;
   P.BN = bn;
-  P.n_kb = G.H / BK;
+  P.n_kb = n_kb;
+  P.ks = ks;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
-  const dim3 grid((G.H + BM - 1) / BM, (G.T + bn - 1) / bn);
-  gemm_lora_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tm_w, tm_x, P);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ks, m_tiles, (G.T + bn - 1) / bn);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = ks;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, P);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_kernel launch");
 }

@@ -101,7 +101,35 @@ struct GemmLaunch {
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
 
+// Programmatic dependent launch: every kernel of the path waits for the kernel before it
+// (griddepcontrol.wait) before touching anything an earlier kernel writes, and only then
+// lets its own dependent start (griddepcontrol.launch_dependents).  So when a kernel starts,
+// the kernel two places before it has completed, and launch latency and prologues overlap.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `st` as a programmatic dependent of the previous kernel in the stream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+int device_sm_count();
+
 // Work-list geometry shared by the segment builder and the gather kernels.
 constexpr int kShrinkTokBlock = 8;   // tokens per shrink unit
 constexpr int kShrinkRankGroup = 8;  // rank columns per shrink unit
-constexpr int kExpandTokBlock = 8;   // tokens per expand unit
+constexpr int kExpandTokBlock = 32;  // tokens per expand unit

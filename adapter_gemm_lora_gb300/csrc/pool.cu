@@ -33,6 +33,17 @@ __global__ void scatter_pages_kernel(const int32_t* __restrict__ ids, const uint
 }
 }  // namespace
 
+int device_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
 int lora_fail(int code, const std::string& msg) {
   g_last_error = msg;
   return code;
@@ -101,6 +112,11 @@ int lora_profile_read(lora_pool* p, int32_t n_kinds, int64_t* launches, double* 
     float t = 0.f;
     cudaError_t e = cudaEventSynchronize(r.stop);
     if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e == cudaErrorInvalidResourceHandle) {   // captured into a graph that has not run yet
+      (void)cudaGetLastError();                  // do not leave it as the runtime's last error
+      e = cudaSuccess;
+      t = 0.f;
+    }
     if (e != cudaSuccess && rc == LORA_OK) rc = lora_cuda_fail(e, "lora_profile_read");
     acc[r.kind] += t;
   }

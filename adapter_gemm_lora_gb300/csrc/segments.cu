@@ -66,6 +66,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   __shared__ int32_t sh_a[33], sh_b[33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = max_adapters + 1;
+  pdl_wait_then_release();
 
   for (int k = tid; k < K; k += kThreads) cnt[k] = 0;
   __syncthreads();
@@ -182,8 +183,9 @@ int launch_segments_build(const lora_pool* p, const int32_t* token_adapter, int3
     if (e != cudaSuccess) return lora_cuda_fail(e, "segments_kernel attribute");
     attr_set = true;
   }
-  segments_kernel<<<1, kThreads, smem, st>>>(token_adapter, T, p->d_rank, p->max_adapters, *seg, p->d_err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(segments_kernel, dim3(1), dim3(kThreads), smem, st, token_adapter, T,
+                             (const int32_t*)p->d_rank, p->max_adapters, *seg, p->d_err);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "segments_kernel launch");
 }
 

@@ -342,7 +342,6 @@ def run_ours(args):
     peaks = load_peaks()
     alg = algorithmic(wl)
     ms_per_step = total_ms_max / steps
-    n_gemm = res["launches"]["gemm"]
     gemm_ms = res["kern_ms"]["gemm"] / max(1, res["kern_sets"] * res["launches_per_graph"]["gemm"])
     shares = {k: v / max(1e-12, sum(res["kern_ms"].values())) for k, v in res["kern_ms"].items()}
     # dominant kernel: the base GEMM; its roof follows the workload's arithmetic intensity
