@@ -32,11 +32,13 @@ LORA_EDEVICE = -7
 LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 16384
 LORA_MAX_TOKENS = 65536
+LORA_NOALLOC_MAX_TOKENS = 128
+LORA_NOALLOC_MAX_H = 8192
 
 EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_adapter_load",
             "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",
             "lora_linear_forward", "lora_status", "lora_pool_stats", "lora_last_error", "lora_pool_destroy",
-            "lora_profile_enable", "lora_profile_read"]
+            "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc"]
 KINDS = ("segments", "shrink", "expand", "gemm", "scatter")
 
 
@@ -90,6 +92,7 @@ def _load():
         "lora_pool_destroy": (None, [VP]),
         "lora_profile_enable": (I32, [VP, I32]),
         "lora_profile_read": (I32, [VP, I32, VP, VP, I32]),
+        "lora_linear_forward_noalloc": (I32, [VP, VP, I32, I32, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -236,3 +239,13 @@ def lora_profile_read(pool, reset: bool = True) -> dict:
     ms = np.zeros(n, dtype=np.float64)
     _check(_load().lora_profile_read(pool, n, _ptr(launches), _ptr(ms), 1 if reset else 0))
     return {k: {"launches": int(launches[i]), "ms": float(ms[i])} for i, k in enumerate(KINDS)}
+
+
+def lora_linear_forward_noalloc(pool, token_adapter_dev, T: int, slot: int, x_dev, W_dev, y_dev, stream=None) -> None:
+    """One projection slot without a caller workspace: the library's static device scratch is used.
+
+    For callers that cannot allocate device memory; at most LORA_NOALLOC_MAX_TOKENS tokens and
+    H <= LORA_NOALLOC_MAX_H.  Calls that overlap on the GPU share the scratch and race.
+    """
+    _check(_load().lora_linear_forward_noalloc(pool, _ptr(token_adapter_dev), T, slot, _ptr(x_dev), _ptr(W_dev),
+                                               _ptr(y_dev), _stream(stream)))

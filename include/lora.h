@@ -215,6 +215,30 @@ int lora_profile_enable(lora_pool* pool, int32_t enable);
 int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, double* ms_host,
                       int32_t reset);
 
+/*
+ * lora_linear_forward_noalloc: the same projection as lora_segments_build followed by
+ * lora_linear_forward, for callers that cannot allocate device memory (no counterpart on the
+ * pages; it exists for library users).  Examples: a plugin whose host runtime owns all device
+ * memory and passes it only inputs and outputs; code recording a CUDA graph while stream
+ * capture forbids cudaMalloc; a latency-critical loop that must not risk the device-wide
+ * synchronisation an allocation can bring.  The segment data and fp32 scratch live in one
+ * static device array of LORA_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits; nothing is allocated per call.
+ *   token_adapter  device int32 [T], -1 = no adapter;  T in 0 .. LORA_NOALLOC_MAX_TOKENS;
+ *   x, W, y        as for lora_linear_forward;  pool H must not exceed LORA_NOALLOC_MAX_H.
+ * The first call on each device looks the array's device address up (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.  All calls share
+ * the array: calls whose work overlaps on the GPU (several streams or host threads) race,
+ * calls ordered on one stream do not.  No value in it needs to start at zero.
+ * Errors: LORA_EINVAL for T or H above the limits (message names the limit) and as for
+ * lora_linear_forward; LORA_ECUDA.
+ */
+#define LORA_NOALLOC_MAX_TOKENS 128
+#define LORA_NOALLOC_MAX_H 8192
+#define LORA_NOALLOC_SCRATCH_BYTES (4608 * 1024)
+int lora_linear_forward_noalloc(lora_pool* pool, const int32_t* token_adapter, int32_t T, int32_t slot,
+                                const void* x, const void* W, void* y, lora_stream_t stream);
+
 /* Free the pool's own host and device memory (not the caller's storage). NULL is ignored. */
 void lora_pool_destroy(lora_pool* pool);
 
