@@ -43,6 +43,7 @@ extern "C" int lora_linear_forward(lora_pool* p, const lora_segments* seg, int32
   L.x = static_cast<const uint16_t*>(x);
   L.delta = delta;
   L.err = p->d_err;
+  L.pdl = !p->prof_on;
   int rc;
   {
     ProfScope prof(p, LORA_KIND_SHRINK, st);
@@ -66,6 +67,7 @@ extern "C" int lora_linear_forward(lora_pool* p, const lora_segments* seg, int32
   G.slot = slot;
   G.n_slots = p->n_slots;
   G.err = p->d_err;
+  G.pdl = !p->prof_on;
   ProfScope prof(p, LORA_KIND_GEMM, st);
   return launch_gemm(G, st);
 }

@@ -107,6 +107,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -207,13 +227,15 @@ __host__ __device__ inline uint32_t tmem_cols_for(int bn) {
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, GemmParams p) {
+gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_y, GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
   const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES, bar_accum = bar_full + 16 * STAGES;
+  const uint32_t bar_delta = bar_accum + 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x;                     // == rank in the (ks, 1, 1) cluster
@@ -229,9 +251,12 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accum, 1);
+    mbar_init(bar_delta, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_d)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_y)) : "memory");
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), ncols);
@@ -245,7 +270,9 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 0) {
     if (lane == 0) {                                  // TMA producer
       const uint32_t tx = A_BYTES + (uint32_t)p.BN * BK * 2;
-      const uint64_t pol_w = policy_evict_first();    // W streams through once
+      // With one token tile (decode batches) W streams through once; otherwise every token tile
+      // re-reads it, so it must not be marked for early eviction.
+      const uint64_t pol_w = gridDim.z == 1 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_x = policy_evict_last();     // x is re-read by every feature tile
       for (int i = 0; i < nk; ++i) {
         const int s = i % STAGES;
@@ -294,8 +321,18 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int row = q * 32 + lane;
   const int n = m0 + row;
   const int cols = p.BN / p.ks;     // token columns this CTA finishes
-  const uint32_t recv = s_base;     // [ks][cols][128] fp32 partials received from the cluster
+  // Stage memory is free now.  Layout: [0, BN*512) fp32 partials received from the cluster,
+  // [ks][cols][128]; this CTA's own slot in it (never written by peers) holds the fp32 delta
+  // sub-tile [cols][128]; the bf16 output sub-tile [cols][128] follows at BN*512 (<= 160 KB).
+  const uint32_t recv = s_base;
+  const uint32_t delta_s = s_base + (uint32_t)(split * cols * BM * 4);
+  const uint32_t y_s = s_base + (uint32_t)(p.BN * BM * 4);
   const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+  const int tc0 = t0 + split * cols;                 // first token column this CTA finishes
+  if (threadIdx.x == 0 && ok) {
+    mbar_arrive_expect_tx(bar_delta, (uint32_t)(cols * BM * 4));
+    tma_load_2d_plain(delta_s, &tm_d, m0, tc0, bar_delta);
+  }
   if (p.ks > 1) {
     cluster_sync_all();             // every CTA is past its mainloop: stage memory may be overwritten
     if (ok) {
@@ -313,6 +350,13 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     }
     cluster_sync_all();             // all partials delivered
   }
+  if (ok) {
+    if (!mbar_wait(bar_delta, 0)) {
+      flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+      ok = false;
+    }
+  }
+  ok = __syncthreads_and(ok) != 0;
   if (ok) {
     for (int cc = h; cc < cols / 32; cc += 2) {
       const int c = split * (cols / 32) + cc;
@@ -337,18 +381,21 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         if (a >= 0) present = p.ptab[((int64_t)a * p.n_slots + p.slot) * kTabStride] >= 0;
       }
       const unsigned pmask = __ballot_sync(0xffffffffu, present);
-      if (n < p.H) {
+      // y_s[col][feature] bf16 for the TMA store; delta_s[col][feature] fp32 from the TMA load
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = tc + i;
-          if (t < p.T) {
-            float acc = __uint_as_float(v[i]);
-            if ((pmask >> i) & 1u) acc += __ldg(p.delta + (int64_t)t * p.H + n);
-            p.y[(int64_t)t * p.H + n] = f32_to_bf16_rn(acc);
-          }
-        }
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t col = (uint32_t)(cc * 32 + i);
+        float acc = __uint_as_float(v[i]);
+        if ((pmask >> i) & 1u) acc += ld_shared_f32(delta_s + (col * BM + row) * 4);
+        st_shared_u16(y_s + (col * BM + row) * 2, f32_to_bf16_rn(acc));
       }
     }
+    fence_proxy_async_shared();     // generic-proxy writes of y_s -> visible to the TMA store
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) {
+    tma_store_2d(&tm_y, m0, tc0, y_s);            // rows past T and features past H are clipped
+    bulk_commit_and_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -384,6 +431,21 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
   return LORA_OK;
 }
 
+// 2-D tensor [rows][inner] row-major without swizzle, box = box_rows x 128 elements.
+int encode_2d_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint32_t esize, uint64_t inner,
+                    uint64_t rows, uint32_t box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * esize};
+  const cuuint32_t box[2] = {(cuuint32_t)BM, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string((int)r));
+  return LORA_OK;
+}
+
 }  // namespace
 
 int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
@@ -407,6 +469,13 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, BM);
   if (rc != LORA_OK) return rc;
   rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
+  if (rc != LORA_OK) return rc;
+  // The delta sub-tile a CTA adds and the output sub-tile it writes: [bn/ks tokens][128 features].
+  CUtensorMap tm_d, tm_y;
+  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T,
+                       (uint32_t)(bn / ks));
+  if (rc != LORA_OK) return rc;
+  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)(bn / ks));
   if (rc != LORA_OK) return rc;
   GemmParams P;
   P.y = G.y;
@@ -434,8 +503,8 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, P);
+  cfg.numAttrs = G.pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, P);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_kernel launch");
 }

@@ -339,7 +339,7 @@ int launch_shrink(const LoraLaunch& L, cudaStream_t st) {
     attr = true;
   }
   const int grid = grid_cap(L.seg->shrink_cap, device_sm_count());
-  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(kShrinkThreads), kShrinkSmem, st, L, *L.seg);
+  cudaError_t e = launch_pdl(L.pdl, shrink_kernel, dim3(grid), dim3(kShrinkThreads), kShrinkSmem, st, L, *L.seg);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "shrink_kernel launch");
 }
@@ -353,7 +353,7 @@ int launch_expand(const LoraLaunch& L, cudaStream_t st) {
   }
   const int n_fc = (L.H + kExpandFeat - 1) / kExpandFeat;
   const int grid = grid_cap(L.seg->expand_cap * n_fc, device_sm_count() * 3);
-  cudaError_t e = launch_pdl(expand_kernel, dim3(grid), dim3(kExpandThreads), kExpandSmem, st, L, *L.seg);
+  cudaError_t e = launch_pdl(L.pdl, expand_kernel, dim3(grid), dim3(kExpandThreads), kExpandSmem, st, L, *L.seg);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "expand_kernel launch");
 }

@@ -61,6 +61,7 @@ struct ProfScope {
   int kind;
   cudaStream_t st;
   int rec = -1;
+  bool capturing = false;
   ProfScope(const lora_pool* pool, int k, cudaStream_t s);
   ~ProfScope();
 };
@@ -73,7 +74,7 @@ int lora_cuda_fail(cudaError_t e, const char* what);
 int launch_scatter_pages(const uint16_t* stage, const int32_t* d_pages, int64_t n_pages, int32_t H,
                          void* pool_dev, cudaStream_t st);
 int launch_segments_build(const lora_pool* pool, const int32_t* token_adapter, int32_t T,
-                          const lora_segments* seg, cudaStream_t st);
+                          const lora_segments* seg, cudaStream_t st, bool pdl);
 
 struct LoraLaunch {
   const uint16_t* pool;
@@ -85,6 +86,7 @@ struct LoraLaunch {
   const uint16_t* x;
   float* delta;
   int32_t* err;
+  bool pdl;
 };
 int launch_shrink(const LoraLaunch& L, cudaStream_t st);
 int launch_expand(const LoraLaunch& L, cudaStream_t st);
@@ -98,6 +100,7 @@ struct GemmLaunch {
   const int32_t* ptab;
   int32_t T, H, slot, n_slots;
   int32_t* err;
+  bool pdl;
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
 
@@ -110,9 +113,11 @@ __device__ __forceinline__ void pdl_wait_then_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Launch `kernel` on `st` as a programmatic dependent of the previous kernel in the stream.
+// Launch `kernel` on `st`, as a programmatic dependent of the previous kernel in the stream
+// when `pdl` is set.  (With per-kernel profiling events recorded between kernels the overlap
+// cannot happen anyway, and such launches are made without the attribute.)
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+inline cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -123,7 +128,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 

@@ -83,14 +83,25 @@ ProfScope::ProfScope(const lora_pool* pool, int k, cudaStream_t s) : p(const_cas
   if (!p->prof_on) return;
   cudaEvent_t a = take_event(p), b = take_event(p);
   if (!a || !b) return;
-  // External records also become event nodes when the stream is being captured into a graph.
-  cudaEventRecordWithFlags(a, st, cudaEventRecordExternal);
+  // While the stream is being captured into a graph, records must be external to become event
+  // nodes of the graph; on an ordinary stream a plain record is the valid form.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  (void)cudaStreamIsCapturing(st, &cs);
+  capturing = cs == cudaStreamCaptureStatusActive;
+  const cudaError_t e = capturing ? cudaEventRecordWithFlags(a, st, cudaEventRecordExternal) : cudaEventRecord(a, st);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();           // profiling must not turn into a launch error
+    return;
+  }
   p->prof_rec.push_back({kind, a, b});
   rec = (int)p->prof_rec.size() - 1;
 }
 
 ProfScope::~ProfScope() {
-  if (rec >= 0) cudaEventRecordWithFlags(p->prof_rec[rec].stop, st, cudaEventRecordExternal);
+  if (rec < 0) return;
+  const cudaEvent_t b = p->prof_rec[rec].stop;
+  const cudaError_t e = capturing ? cudaEventRecordWithFlags(b, st, cudaEventRecordExternal) : cudaEventRecord(b, st);
+  if (e != cudaSuccess) (void)cudaGetLastError();
 }
 
 extern "C" {

@@ -174,7 +174,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
 }  // namespace
 
 int launch_segments_build(const lora_pool* p, const int32_t* token_adapter, int32_t T, const lora_segments* seg,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
   const size_t smem = (size_t)(p->max_adapters + 1) * sizeof(int32_t);
   static bool attr_set = false;
   if (!attr_set) {
@@ -183,7 +183,7 @@ int launch_segments_build(const lora_pool* p, const int32_t* token_adapter, int3
     if (e != cudaSuccess) return lora_cuda_fail(e, "segments_kernel attribute");
     attr_set = true;
   }
-  cudaError_t e = launch_pdl(segments_kernel, dim3(1), dim3(kThreads), smem, st, token_adapter, T,
+  cudaError_t e = launch_pdl(pdl, segments_kernel, dim3(1), dim3(kThreads), smem, st, token_adapter, T,
                              (const int32_t*)p->d_rank, p->max_adapters, *seg, p->d_err);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "segments_kernel launch");
@@ -198,7 +198,7 @@ extern "C" int lora_segments_build(lora_pool* p, const int32_t* token_adapter, i
   int rc;
   {
     ProfScope prof(p, LORA_KIND_SEGMENTS, reinterpret_cast<cudaStream_t>(stream));
-    rc = launch_segments_build(p, token_adapter, T, seg, reinterpret_cast<cudaStream_t>(stream));
+    rc = launch_segments_build(p, token_adapter, T, seg, reinterpret_cast<cudaStream_t>(stream), !p->prof_on);
   }
   if (rc == LORA_OK) seg->T = T;
   return rc;
