@@ -14,16 +14,18 @@
 // column = token.  That suits the epilogue: a warp covers 32 consecutive features of
 // one token, so delta loads and y stores are contiguous along the feature dimension.
 //
-// Per CTA: one 128 x BN output tile over a slice of K.  Warp 0 issues TMA loads into a
-// 4-stage ring, warp 1 owns TMEM and a single thread issues the MMAs, then all 8 warps
+// Per CTA: one 128 x BN output tile over the full K.  Warp 0 issues TMA loads into a ring
+// of up to 8 stages (each 1, 2 or 4 K chunks of 64, so that a stage carries >= ~40 KB), warp 1 owns TMEM and a single thread issues the MMAs, then all 8 warps
 // drain TMEM (warp w reads TMEM lanes 32*(w%4) .. +31, half the columns each).
-// Small grids (decode batches: H/128 x 1 tiles for 152 SMs) split K over the CTAs of a
-// thread-block cluster; each CTA then owns BN/ks token columns, receives the other CTAs'
-// fp32 partials for them through distributed shared memory, and sums them in split order
-// (deterministic) before the epilogue.  The mainloop reads only x and W, so the kernel is
+// Token tiles shrink (down to 32 tokens) until the grid fills the SMs; CTAs that share a
+// feature tile form a thread-block cluster of up to 4 along the token dimension, and each
+// loads 1/CN of the W tile and multicasts it to the whole cluster (stages are released
+// cluster-wide by multicast tcgen05.commit), so W crosses L2 once per cluster.
+// The epilogue stages the fp32 delta sub-tile (one TMA load) and the bf16 output (one TMA
+// store) through the freed stage memory.  The mainloop reads only x and W, so the kernel is
 // launched as a programmatic dependent of the LoRA kernels before it and waits for them
 // (griddepcontrol.wait) only before its epilogue reads the delta.
-// Every mbarrier wait is bounded (~2 s); on expiry the CTA raises the device error word,
+// Every mbarrier wait is bounded (~2 s of SM cycles); on expiry the CTA raises the device error word,
 // skips the rest of its work and frees TMEM before returning.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -39,14 +41,12 @@ namespace {
 constexpr int BM = 128;          // output features per tile (MMA M)
 constexpr int BK = 64;           // K elements per stage: one 128-byte swizzle atom wide
 constexpr int MAX_BN = 256;      // tokens per tile (MMA N)
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = MAX_BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGE_AREA = 192 * 1024;        // ring of stages; reused by the epilogue
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGE_AREA + BAR_BYTES;
 constexpr int THREADS = 256;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemmParams {
   uint16_t* y;
@@ -54,7 +54,7 @@ struct GemmParams {
   const int32_t* tok_adapter;
   const int32_t* ptab;
   int32_t* err;
-  int32_t T, H, BN, n_kb, ks, slot, n_slots;
+  int32_t T, H, BN, n_kb, kc, stages, cn, slot, n_slots;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -75,26 +75,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)   // suspend-time hint (ns); the phase completing wakes it
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase of the given parity to complete; false if ~2 s pass first.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of the given parity to complete; false if the wait runs out.  The bound
+// is counted with the SM's own cycle counter (clock64): it is cheap to read, unlike the global
+// timer, whose read latency would otherwise land on every pipeline step.  4e9 cycles is about
+// 2 s at the maximum SM clock.
+constexpr long long kWaitLimitCycles = 4000000000ll;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long c0 = clock64();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > kWaitLimitCycles) return false;
   }
 }
 
@@ -105,6 +105,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+// The same box lands at the same shared-memory offset in every CTA of `mask` and signals each
+// CTA's mbarrier at the same offset.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                                      uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -184,6 +194,18 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// The same, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
 
 // 32 lanes x 32 consecutive columns of 32-bit TMEM data: thread i gets lane (base + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -232,23 +254,28 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
-  const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES, bar_accum = bar_full + 16 * STAGES;
-  const uint32_t bar_delta = bar_accum + 8;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGE_AREA);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 2);
+  const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * MAX_STAGES;
+  const uint32_t bar_accum = bar_full + 16 * MAX_STAGES, bar_delta = bar_accum + 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x;                     // == rank in the (ks, 1, 1) cluster
   const int m0 = blockIdx.y * BM;
   const int t0 = blockIdx.z * p.BN;
-  const int kb0 = split * p.n_kb / p.ks, kb1 = (split + 1) * p.n_kb / p.ks;
-  const int nk = kb1 - kb0;
+  const int cn = p.cn;                                  // CTAs sharing the W tile (cluster along tokens)
+  const uint32_t crank = cn > 1 ? cluster_ctarank() : 0;
+  const uint16_t cmask = (uint16_t)((1u << cn) - 1u);
+  const int stages = p.stages;
+  const int kc = p.kc;                                  // 64-wide K chunks per stage
+  const uint32_t xb = (uint32_t)(p.BN * BK * 2);        // one x chunk
+  const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
+  const int nk = p.n_kb / kc;                           // stages' worth of K (n_kb is a multiple of kc)
   const uint32_t ncols = tmem_cols_for(p.BN);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, (uint32_t)cn);      // one release per CTA of the cluster
     }
     mbar_init(bar_accum, 1);
     mbar_init(bar_delta, 1);
@@ -265,46 +292,62 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (cn > 1) cluster_sync_all();                       // peers' barriers exist before anything targets them
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {                                  // TMA producer
-      const uint32_t tx = A_BYTES + (uint32_t)p.BN * BK * 2;
-      // With one token tile (decode batches) W streams through once; otherwise every token tile
-      // re-reads it, so it must not be marked for early eviction.
-      const uint64_t pol_w = gridDim.z == 1 ? policy_evict_first() : policy_evict_last();
-      const uint64_t pol_x = policy_evict_last();     // x is re-read by every feature tile
+    if (lane == 0) {                                    // TMA producer
+      const uint32_t tx = stage_bytes;                  // whole W tile (cn multicast slices) + own x tile
+      // When one cluster covers every token tile (decode batches) W crosses L2 once; otherwise
+      // other clusters re-read it, so it must not be marked for early eviction.
+      const uint64_t pol_w = (int)gridDim.z == cn ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_x = policy_evict_last();       // x is re-read by every feature tile
+      const int w_rows = BM / cn;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {    // released by every CTA of the cluster
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
         }
         mbar_arrive_expect_tx(bar_full + 8 * s, tx);
-        const int kc = (kb0 + i) * BK;
-        tma_load_2d(s_base + s * STAGE_BYTES, &tm_w, kc, m0, bar_full + 8 * s, pol_w);
-        tma_load_2d(s_base + s * STAGE_BYTES + A_BYTES, &tm_x, kc, t0, bar_full + 8 * s, pol_x);
+        const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+        for (int c = 0; c < kc; ++c) {
+          const int kx = (i * kc + c) * BK;
+          const uint32_t wdst = st + (uint32_t)c * A_BYTES;
+          if (cn > 1)
+            tma_load_2d_multicast(wdst + crank * (uint32_t)(w_rows * BK * 2), &tm_w, kx, m0 + (int)crank * w_rows,
+                                  bar_full + 8 * s, cmask, pol_w);
+          else
+            tma_load_2d(wdst, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
+          tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {                                  // MMA issuer
+    if (lane == 0) {                                    // MMA issuer
       const uint32_t idesc = make_idesc_bf16(BM, p.BN);
       for (int i = 0; i < nk; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
+        const int s = i % stages;
+        const uint32_t ph = (i / stages) & 1;
         if (!mbar_wait(bar_full + 8 * s, ph)) {
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_kmajor_desc(s_base + s * STAGE_BYTES);
-        const uint64_t bd = sw128_kmajor_desc(s_base + s * STAGE_BYTES + A_BYTES);
+        const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+        for (int c = 0; c < kc; ++c) {
+          const uint64_t ad = sw128_kmajor_desc(st + (uint32_t)c * A_BYTES);
+          const uint64_t bd = sw128_kmajor_desc(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)             // 16-element K steps = 32 bytes = 2 descriptor units
-          mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
-        mma_commit(bar_empty + 8 * s);
+          for (int k = 0; k < BK / 16; ++k)             // 16-element K steps = 32 bytes = 2 descriptor units
+            mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
+        }
+        if (cn > 1)
+          mma_commit_multicast(bar_empty + 8 * s, cmask);
+        else
+          mma_commit(bar_empty + 8 * s);
       }
       mma_commit(bar_accum);
     }
@@ -319,60 +362,25 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   pdl_wait_then_release();         // the delta and validated ids come from the kernels before this one
   const int q = warp & 3, h = warp >> 2;
   const int row = q * 32 + lane;
-  const int n = m0 + row;
-  const int cols = p.BN / p.ks;     // token columns this CTA finishes
-  // Stage memory is free now.  Layout: [0, BN*512) fp32 partials received from the cluster,
-  // [ks][cols][128]; this CTA's own slot in it (never written by peers) holds the fp32 delta
-  // sub-tile [cols][128]; the bf16 output sub-tile [cols][128] follows at BN*512 (<= 160 KB).
-  const uint32_t recv = s_base;
-  const uint32_t delta_s = s_base + (uint32_t)(split * cols * BM * 4);
+  // Stage memory is free now (every multicast into it belonged to a k-block consumed above):
+  // the fp32 delta tile [BN][128] at 0, the bf16 output tile [BN][128] after it (<= 192 KB).
+  const uint32_t delta_s = s_base;
   const uint32_t y_s = s_base + (uint32_t)(p.BN * BM * 4);
   const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
-  const int tc0 = t0 + split * cols;                 // first token column this CTA finishes
   if (threadIdx.x == 0 && ok) {
-    mbar_arrive_expect_tx(bar_delta, (uint32_t)(cols * BM * 4));
-    tma_load_2d_plain(delta_s, &tm_d, m0, tc0, bar_delta);
+    mbar_arrive_expect_tx(bar_delta, (uint32_t)(p.BN * BM * 4));
+    tma_load_2d_plain(delta_s, &tm_d, m0, t0, bar_delta);
   }
-  if (p.ks > 1) {
-    cluster_sync_all();             // every CTA is past its mainloop: stage memory may be overwritten
-    if (ok) {
-      for (int c = h; c < p.BN / 32; c += 2) {
-        const int owner = (c * 32) / cols;
-        if (owner == split) continue;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
-        tmem_ld_wait();
-        const uint32_t base = recv + (uint32_t)(((split * cols + c * 32 - owner * cols) * BM + row) * 4);
-        const uint32_t remote = map_to_cta(base, (uint32_t)owner);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) st_cluster_f32(remote + (uint32_t)(i * BM * 4), __uint_as_float(v[i]));
-      }
-    }
-    cluster_sync_all();             // all partials delivered
-  }
-  if (ok) {
-    if (!mbar_wait(bar_delta, 0)) {
-      flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
-      ok = false;
-    }
+  if (ok && !mbar_wait(bar_delta, 0)) {
+    flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+    ok = false;
   }
   ok = __syncthreads_and(ok) != 0;
   if (ok) {
-    for (int cc = h; cc < cols / 32; cc += 2) {
-      const int c = split * (cols / 32) + cc;
+    for (int c = h; c < p.BN / 32; c += 2) {
       uint32_t v[32];
       tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
       tmem_ld_wait();
-      if (p.ks > 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float sum = 0.f;
-          for (int src = 0; src < p.ks; ++src)
-            sum += src == split ? __uint_as_float(v[i])
-                                : ld_shared_f32(recv + (uint32_t)(((src * cols + cc * 32 + i) * BM + row) * 4));
-          v[i] = __float_as_uint(sum);
-        }
-      }
       const int tc = t0 + c * 32;
       const int tl = tc + lane;
       int present = 0;
@@ -384,7 +392,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       // y_s[col][feature] bf16 for the TMA store; delta_s[col][feature] fp32 from the TMA load
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint32_t col = (uint32_t)(cc * 32 + i);
+        const uint32_t col = (uint32_t)(c * 32 + i);
         float acc = __uint_as_float(v[i]);
         if ((pmask >> i) & 1u) acc += ld_shared_f32(delta_s + (col * BM + row) * 4);
         st_shared_u16(y_s + (col * BM + row) * 2, f32_to_bf16_rn(acc));
@@ -394,12 +402,13 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   }
   __syncthreads();
   if (threadIdx.x == 0 && ok) {
-    tma_store_2d(&tm_y, m0, tc0, y_s);            // rows past T and features past H are clipped
+    tma_store_2d(&tm_y, m0, t0, y_s);             // rows past T and features past H are clipped
     bulk_commit_and_wait_all();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
+  if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
 }
 
 // ---- host side --------------------------------------------------------------------------
@@ -456,26 +465,38 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
     attr_set = true;
   }
   const int n_sm = device_sm_count();
-  const int n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
+  const int m_tiles = (G.H + BM - 1) / BM;
+  // Token tiles: as few as possible (<= 256 tokens each), but enough to fill about 3/4 of the
+  // SMs when the feature tiles alone do not (decode batches), down to 32-token tiles.
+  int n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
+  const int want = (3 * n_sm / 4 + m_tiles - 1) / m_tiles;
+  const int max_tiles = (G.T + 31) / 32;
+  if (n_tiles < want) n_tiles = want < max_tiles ? want : max_tiles;
   int bn = (G.T + n_tiles - 1) / n_tiles;
   bn = ((bn + 31) / 32) * 32;
   if (bn > MAX_BN) bn = MAX_BN;
-  const int m_tiles = (G.H + BM - 1) / BM;
+  n_tiles = (G.T + bn - 1) / bn;
+  // Wide token tiles share each W tile across a cluster (multicast); for narrow tiles the
+  // per-SM shared-memory fill rate, not L2, is the limit, and the cluster only adds coupling.
+  const int cn = bn < 128 ? 1 : (n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1));
+  // Each pipeline stage costs a fixed handshake on top of its data, and a CTA's TMA fill rate is
+  // bounded, so stages are made large: up to 4 K chunks of 64, at most 96 KB (>= 2 stages).
   const int n_kb = G.H / BK;
-  // Split K over a cluster while the grid would leave most SMs idle.
-  int ks = 1;
-  while (ks < 8 && m_tiles * n_tiles * ks * 2 <= n_sm && n_kb / (ks * 2) >= 4 && bn % (32 * ks * 2) == 0) ks *= 2;
-  CUtensorMap tm_w, tm_x;
-  int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, BM);
+  const int chunk_bytes = A_BYTES + bn * BK * 2;
+  int kc = 1;                       // wide tiles are MMA-bound: one chunk per stage
+  while (bn < 128 && kc < 4 && 2 * kc * chunk_bytes <= 96 * 1024 && n_kb % (2 * kc) == 0) kc *= 2;
+  const int stage_bytes = kc * chunk_bytes;
+  int stages = STAGE_AREA / stage_bytes;
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
+  CUtensorMap tm_w, tm_x, tm_d, tm_y;
+  int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)(BM / cn));
   if (rc != LORA_OK) return rc;
   rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
   if (rc != LORA_OK) return rc;
-  // The delta sub-tile a CTA adds and the output sub-tile it writes: [bn/ks tokens][128 features].
-  CUtensorMap tm_d, tm_y;
-  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T,
-                       (uint32_t)(bn / ks));
+  // The delta tile the epilogue adds and the output tile it writes: [bn tokens][128 features].
+  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
   if (rc != LORA_OK) return rc;
-  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)(bn / ks));
+  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
   if (rc != LORA_OK) return rc;
   GemmParams P;
   P.y = G.y;
@@ -487,19 +508,21 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.H = G.H;
   P.BN = bn;
   P.n_kb = n_kb;
-  P.ks = ks;
+  P.kc = kc;
+  P.stages = stages;
+  P.cn = cn;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ks, m_tiles, (G.T + bn - 1) / bn);
+  cfg.gridDim = dim3(1, m_tiles, n_tiles);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = ks;
+  attrs[0].val.clusterDim.x = 1;
   attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  attrs[0].val.clusterDim.z = cn;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;

@@ -137,4 +137,4 @@ int device_sm_count();
 // Work-list geometry shared by the segment builder and the gather kernels.
 constexpr int kShrinkTokBlock = 8;   // tokens per shrink unit
 constexpr int kShrinkRankGroup = 8;  // rank columns per shrink unit
-constexpr int kExpandTokBlock = 32;  // tokens per expand unit
+constexpr int kExpandTokBlock = 8;   // tokens per expand unit

@@ -6,10 +6,10 @@
 // token.  Output order: ascending adapter id, ties by token index; tokens without an
 // adapter (-1) first and outside every segment.
 //
-// One CTA of 1024 threads: a shared-memory histogram over adapter ids, a block scan that
-// turns counts into run starts and lists the non-empty adapters, then a stable scatter in
-// chunks of 1024 tokens (warp-level match for ranks inside a warp, warps in order), and
-// finally the work lists of the shrink and expand kernels.
+// One CTA of 1024 threads: a shared-memory histogram over adapter ids (with each used
+// adapter's rank), one block scan that turns counts into run starts, segment indices and the
+// offsets of the shrink and expand work lists (written right away), then a stable scatter in
+// chunks of 1024 tokens (warp-level match for ranks inside a warp, warps in order).
 #include <cuda_runtime.h>
 
 #include "lora_internal.h"
@@ -24,59 +24,70 @@ __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
   atomicOr(err + 1, bits);
 }
 
-// Exclusive block scan of two int32 values per thread; returns the totals in *tot0/*tot1.
-__device__ __forceinline__ void block_exclusive_scan2(int32_t& a, int32_t& b, int32_t* sh_a, int32_t* sh_b,
-                                                      int32_t* tot_a, int32_t* tot_b) {
+// Exclusive block scan of four int32 values per thread; totals land in tot[0..3].
+__device__ __forceinline__ void block_exclusive_scan4(int32_t (&v)[4], int32_t (*sh)[33], int32_t (&tot)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int32_t ia = a, ib = b;
+  int32_t inc[4];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int32_t va = __shfl_up_sync(0xffffffffu, ia, o);
-    int32_t vb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) { ia += va; ib += vb; }
-  }
-  if (lane == 31) { sh_a[warp] = ia; sh_b[warp] = ib; }
-  __syncthreads();
-  if (warp == 0) {
-    int32_t wa = sh_a[lane], wb = sh_b[lane];
-    int32_t sa = wa, sb = wb;
+  for (int q = 0; q < 4; ++q) {
+    inc[q] = v[q];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int32_t va = __shfl_up_sync(0xffffffffu, sa, o);
-      int32_t vb = __shfl_up_sync(0xffffffffu, sb, o);
-      if (lane >= o) { sa += va; sb += vb; }
+      const int32_t t = __shfl_up_sync(0xffffffffu, inc[q], o);
+      if (lane >= o) inc[q] += t;
     }
-    sh_a[lane] = sa - wa;   // exclusive prefix of warp totals
-    sh_b[lane] = sb - wb;
-    if (lane == 31) { sh_a[32] = sa; sh_b[32] = sb; }
+    if (lane == 31) sh[q][warp] = inc[q];
   }
   __syncthreads();
-  const int32_t ea = sh_a[warp] + ia - a, eb = sh_b[warp] + ib - b;
-  *tot_a = sh_a[32];
-  *tot_b = sh_b[32];
-  a = ea;
-  b = eb;
+  if (warp == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int32_t w = sh[q][lane];
+      int32_t x = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += t;
+      }
+      sh[q][lane] = x - w;              // exclusive prefix of the warp totals
+      if (lane == 31) sh[q][32] = x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[q] = sh[q][warp] + inc[q] - v[q];
+    tot[q] = sh[q][32];
+  }
   __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int32_t* __restrict__ rank,
                 int32_t max_adapters, lora_segments seg, int32_t* __restrict__ err) {
-  extern __shared__ int32_t cnt[];           // [max_adapters + 1], key = adapter id + 1 (0 = none)
-  __shared__ int32_t sh_a[33], sh_b[33];
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                          // [K] tokens per key, then run starts / write cursors
+  int32_t* krank = sm + (max_adapters + 1);   // [K] rank of the key's adapter
+  __shared__ int32_t sh_scan[4][33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = max_adapters + 1;
+  const int K = max_adapters + 1;              // key = adapter id + 1; key 0 = no adapter
   pdl_wait_then_release();
 
   for (int k = tid; k < K; k += kThreads) cnt[k] = 0;
   __syncthreads();
 
-  // 1. validate ids and count tokens per key
+  // 1. validate ids, count tokens per key, remember each used adapter's rank
   for (int t = tid; t < T; t += kThreads) {
     const int32_t a = token_adapter[t];
     int32_t key = 0;
-    if (a >= 0 && a < max_adapters && rank[a] > 0) {
-      key = a + 1;
+    if (a >= 0 && a < max_adapters) {
+      const int32_t r = rank[a];
+      if (r > 0) {
+        key = a + 1;
+        krank[key] = r;
+      } else {
+        flag_error(err, LORA_DEV_UNKNOWN_ADAPTER);
+      }
     } else if (a != -1) {
       flag_error(err, LORA_DEV_UNKNOWN_ADAPTER);
     }
@@ -85,35 +96,60 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   }
   __syncthreads();
 
-  // 2. run starts per key, list of non-empty adapters (the segments)
+  // 2. one scan gives run starts, segment indices and both work-list offsets; each thread then
+  //    writes the segments and work units of its own keys
   const int per = (K + kThreads - 1) / kThreads;
   const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
-  int32_t csum = 0, nz = 0;
+  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, expand units, shrink units
   for (int k = k_lo; k < k_hi; ++k) {
-    csum += cnt[k];
-    nz += (k > 0 && cnt[k] > 0);
+    const int32_t c = cnt[k];
+    v[0] += c;
+    if (k > 0 && c > 0) {
+      const int32_t nb_e = (c + kExpandTokBlock - 1) / kExpandTokBlock;
+      const int32_t nb_s = (c + kShrinkTokBlock - 1) / kShrinkTokBlock;
+      v[1] += 1;
+      v[2] += nb_e;
+      v[3] += nb_s * ((krank[k] + kShrinkRankGroup - 1) / kShrinkRankGroup);
+    }
   }
-  int32_t tot_c, tot_nz;
-  block_exclusive_scan2(csum, nz, sh_a, sh_b, &tot_c, &tot_nz);
+  int32_t tot[4];
+  block_exclusive_scan4(v, sh_scan, tot);
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     if (k > 0 && c > 0) {
-      seg.seg_off[nz] = csum;
-      seg.seg_adapter[nz] = k - 1;
-      ++nz;
+      const int32_t sidx = v[1];
+      seg.seg_off[sidx] = v[0];
+      seg.seg_adapter[sidx] = k - 1;
+      const int32_t nb_e = (c + kExpandTokBlock - 1) / kExpandTokBlock;
+      for (int b = 0; b < nb_e; ++b, ++v[2]) {
+        seg.expand_work[2 * v[2]] = sidx;
+        seg.expand_work[2 * v[2] + 1] = b;
+      }
+      const int32_t nb_s = (c + kShrinkTokBlock - 1) / kShrinkTokBlock;
+      const int32_t ng = (krank[k] + kShrinkRankGroup - 1) / kShrinkRankGroup;
+      for (int b = 0; b < nb_s; ++b)
+        for (int gi = 0; gi < ng; ++gi, ++v[3]) {
+          seg.shrink_work[4 * v[3]] = sidx;
+          seg.shrink_work[4 * v[3] + 1] = b;
+          seg.shrink_work[4 * v[3] + 2] = gi;
+          seg.shrink_work[4 * v[3] + 3] = 0;
+        }
+      ++v[1];
     }
-    cnt[k] = csum;      // becomes the running write position of key k
-    csum += c;
+    cnt[k] = v[0];                             // becomes the running write position of key k
+    v[0] += c;
   }
-  const int32_t S = tot_nz;
+  const int32_t S = tot[1];
   if (tid == 0) {
     seg.seg_off[S] = T;
     if (S == 0) seg.seg_off[0] = T;
     *seg.n_seg = S;
+    *seg.n_expand = tot[2];
+    *seg.n_shrink = tot[3];
   }
   __syncthreads();
 
-  // 3. stable scatter, 1024 tokens at a time; warps take their turn in index order
+  // 3. stable scatter, 1024 tokens at a time; the warps holding tokens take turns in index order
   for (int base_t = 0; base_t < T; base_t += kThreads) {
     const int t = base_t + tid;
     const bool valid = t < T;
@@ -121,7 +157,8 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     const int lrank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
-    for (int w = 0; w < kWarps; ++w) {
+    const int n_warps = min(kWarps, (T - base_t + 31) / 32);
+    for (int w = 0; w < n_warps; ++w) {
       if (warp == w) {
         int32_t pos = 0;
         if (valid && lane == leader) {
@@ -134,52 +171,17 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
       __syncthreads();
     }
   }
-
-  // 4. work lists: expand units (segment, token block); shrink units (segment, token block, rank group)
-  const int sper = (S + kThreads - 1) / kThreads;
-  const int s_lo = min(S, tid * sper), s_hi = min(S, s_lo + sper);
-  int32_t ne = 0, ns = 0;
-  for (int s = s_lo; s < s_hi; ++s) {
-    const int32_t n = seg.seg_off[s + 1] - seg.seg_off[s];
-    const int32_t r = rank[seg.seg_adapter[s]];
-    ne += (n + kExpandTokBlock - 1) / kExpandTokBlock;
-    ns += ((n + kShrinkTokBlock - 1) / kShrinkTokBlock) * ((r + kShrinkRankGroup - 1) / kShrinkRankGroup);
-  }
-  int32_t tot_e, tot_s;
-  block_exclusive_scan2(ne, ns, sh_a, sh_b, &tot_e, &tot_s);
-  for (int s = s_lo; s < s_hi; ++s) {
-    const int32_t n = seg.seg_off[s + 1] - seg.seg_off[s];
-    const int32_t r = rank[seg.seg_adapter[s]];
-    const int32_t nbe = (n + kExpandTokBlock - 1) / kExpandTokBlock;
-    for (int b = 0; b < nbe; ++b, ++ne) {
-      seg.expand_work[2 * ne] = s;
-      seg.expand_work[2 * ne + 1] = b;
-    }
-    const int32_t nbs = (n + kShrinkTokBlock - 1) / kShrinkTokBlock;
-    const int32_t ng = (r + kShrinkRankGroup - 1) / kShrinkRankGroup;
-    for (int b = 0; b < nbs; ++b)
-      for (int g = 0; g < ng; ++g, ++ns) {
-        seg.shrink_work[4 * ns] = s;
-        seg.shrink_work[4 * ns + 1] = b;
-        seg.shrink_work[4 * ns + 2] = g;
-        seg.shrink_work[4 * ns + 3] = 0;
-      }
-  }
-  if (tid == 0) {
-    *seg.n_expand = tot_e;
-    *seg.n_shrink = tot_s;
-  }
 }
 
 }  // namespace
 
 int launch_segments_build(const lora_pool* p, const int32_t* token_adapter, int32_t T, const lora_segments* seg,
                           cudaStream_t st, bool pdl) {
-  const size_t smem = (size_t)(p->max_adapters + 1) * sizeof(int32_t);
+  const size_t smem = 2 * (size_t)(p->max_adapters + 1) * sizeof(int32_t);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((LORA_MAX_ADAPTERS + 1) * sizeof(int32_t)));
+                                         (int)(2 * (LORA_MAX_ADAPTERS + 1) * sizeof(int32_t)));
     if (e != cudaSuccess) return lora_cuda_fail(e, "segments_kernel attribute");
     attr_set = true;
   }
