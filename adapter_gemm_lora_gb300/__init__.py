@@ -39,7 +39,7 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",
             "lora_linear_forward", "lora_status", "lora_pool_stats", "lora_last_error", "lora_pool_destroy",
             "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc"]
-KINDS = ("segments", "shrink", "expand", "gemm", "scatter")
+KINDS = ("segments", "delta", "gemm", "scatter")
 
 
 class LoraError(RuntimeError):
@@ -52,10 +52,9 @@ class LoraError(RuntimeError):
 class lora_segments(ctypes.Structure):
     _fields_ = [("T_max", ctypes.c_int32), ("T", ctypes.c_int32), ("max_seg", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("perm", ctypes.c_void_p), ("seg_off", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
-                ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("shrink_work", ctypes.c_void_p),
-                ("n_shrink", ctypes.c_void_p), ("expand_work", ctypes.c_void_p), ("n_expand", ctypes.c_void_p),
-                ("shrink_cap", ctypes.c_int32), ("expand_cap", ctypes.c_int32),
-                ("s", ctypes.c_void_p), ("delta", ctypes.c_void_p)]
+                ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("units", ctypes.c_void_p),
+                ("n_units", ctypes.c_void_p), ("unit_cap", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("delta", ctypes.c_void_p)]
 
 
 class lora_pool_stats_t(ctypes.Structure):

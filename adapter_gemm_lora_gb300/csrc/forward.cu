@@ -2,9 +2,9 @@
 //
 // "S-LoRA, in depth", section "Merge or keep adapters separate": y = xW + (xA)B per token,
 // W shared, A and B the token's own adapter.  Three kernels on the caller's stream:
-//   1. shrink   s = x A        per segment of tokens sharing an adapter (paged gather)
-//   2. expand   delta = s B    per segment (paged gather), fp32
-//   3. base GEMM x W^T on tcgen05, epilogue y = bf16_rne(acc + delta)
+//   1. LoRA delta: s = x A, then delta = s B, per run of tokens sharing an adapter (paged
+//      gathers, fused in one kernel; s stays on chip)
+//   2. base GEMM x W^T on tcgen05, epilogue y = bf16_rne(acc + delta)
 #include <cuda_runtime.h>
 
 #include "lora_internal.h"
@@ -46,12 +46,8 @@ extern "C" int lora_linear_forward(lora_pool* p, const lora_segments* seg, int32
   L.pdl = !p->prof_on;
   int rc;
   {
-    ProfScope prof(p, LORA_KIND_SHRINK, st);
-    rc = launch_shrink(L, st);
-  }
-  if (rc == LORA_OK) {
-    ProfScope prof(p, LORA_KIND_EXPAND, st);
-    rc = launch_expand(L, st);
+    ProfScope prof(p, LORA_KIND_DELTA, st);
+    rc = launch_lora_delta(L, st);
   }
   if (rc != LORA_OK) return rc;
 

@@ -1,19 +1,34 @@
-// Paged-gather shrink and expand: the two skinny products of the unmerged LoRA term.
+// The LoRA delta of one projection slot: the two skinny products of the unmerged term.
 //
 // "S-LoRA, in depth", section "Merge or keep adapters separate": besides the shared xW,
-// each token needs (xA)B for its own adapter, two skinny matmuls.  Section "Kernels for a
-// batch of mixed ranks": A and B sit in scattered pool pages and ranks differ inside one
-// batch, so the kernels gather pages through the page table.
+// each token needs (xA)B for its own adapter.  Section "Kernels for a batch of mixed ranks":
+// A and B sit in scattered pool pages and ranks differ inside one batch, so both products
+// gather their operands through the page table.  Here they run fused in one kernel:
+//   shrink  s[t, j]     = sum_k x[t, k] * A[k, j]        (A page j = column j of A, H values)
+//   expand  delta[t, n] = sum_j s[t, j] * B[j, n]        (B page j = row j of B, H values)
 //
-// Both kernels walk work lists built per batch by the segment builder, so each unit
-// serves a run of tokens that share one adapter and every page is fetched once per unit:
-//   shrink  s[t, j]     = sum_k x[t, k] * A[k, j]   unit = (segment, 8 tokens, 8 ranks)
-//   expand  delta[t, n] = sum_j s[t, j] * B[j, n]    unit = (segment, 32 tokens, 1024 features)
-// A page gather is latency-bound unless many bytes are in flight: every lane issues 8 to 16
-// independent 16-byte loads before using any of them, and no barrier sits inside a unit, so
-// all resident warps keep the memory system busy.  bf16 inputs, fp32 accumulation, and a
-// fixed summation order that depends neither on page placement nor on the other tokens of
-// the batch.
+// Work unit: up to 16 tokens of one segment (tokens that share an adapter), handled by a
+// cluster of 4 CTAs.  CTA q owns one quarter of the feature range, [q H/4, (q+1) H/4), for
+// both products: it reads that quarter of the unit's token rows of x, of all r A pages and of
+// all r B pages, and nothing else.  The shrink over its quarter gives partial sums of s; the
+// four partials are exchanged through distributed shared memory and added in a fixed order,
+// so every CTA holds the same complete s.  The expand then writes the CTA's quarter of delta.
+//
+// Data movement: one producer warp streams page-row slices (at most 1024 features, 2 KB) into a
+// ring of 5 shared-memory stages with TMA bulk copies (cp.async.bulk), 16 rows per stage:
+// the x rows of the unit, then the A pages 16 at a time, then the B pages 16 at a time.  Up to
+// 160 KB per SM is in flight, so the page gather runs at memory speed without register
+// staging.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
+// level bf16 MMA (m16n8k16, fp32 accumulation), feeding operands with ldmatrix straight from
+// the staged page rows: a unit holds 16 tokens at most, below the 64-row minimum tile of the
+// asynchronous tcgen05 MMA, while ldmatrix takes any row addresses, which is what a page
+// gather produces.  The MMAs exist only to keep the 16-way reuse of every loaded byte off the
+// CUDA cores; the kernel is bound by the bytes it gathers.
+//
+// Precision: bf16 inputs, exact products, fp32 accumulation.  s is passed to the expand as
+// two bf16 terms (s = hi + lo, with hi = bf16(s), lo = bf16(s - hi)), which keeps 16 bits of
+// its mantissa.  The order of every sum is fixed and depends neither on page placement nor on
+// the other tokens of the batch.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,276 +36,504 @@
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kCluster = 4;                    // CTAs per unit, one feature quarter each
+constexpr int kUnitTok = kUnitTokens;         // tokens per unit (16)
+constexpr int kFB = 1024;                      // features per stage row (one feature block)
+constexpr int kRows = 16;                      // rows per stage
+constexpr int kStages = 5;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;      // + one producer warp
+// Stage rows are padded by 16 bytes so that the 8 rows an ldmatrix phase reads fall in 8
+// different 16-byte bank groups.
+constexpr int kSlotBytes = kRows * (kFB * 2 + 16);
+constexpr int kSbPitch = LORA_MAX_RANK + 8;    // bf16 elements per token row of s (hi or lo)
+// shared memory layout (dynamic)
+constexpr int kOffRing = 0;
+constexpr int kOffPart = kOffRing + kStages * kSlotBytes;                    // [8 warps][16][16] f32
+constexpr int kOffExch = kOffPart + kConsumerWarps * 16 * 16 * 4;            // [2][4][64][16] f32
+constexpr int kOffSb = kOffExch + 2 * kCluster * LORA_MAX_RANK * kUnitTok * 4;  // [2][16][kSbPitch] bf16
+constexpr int kOffBar = kOffSb + 2 * kUnitTok * kSbPitch * 2;
+constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
+static_assert(kUnitTok == 16, "the MMA tiling assumes 16 tokens per unit");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffSb % 16 == 0 && kOffBar % 8 == 0, "alignment");
 
 __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
   atomicCAS(err, 0, LORA_EDEVICE);
   atomicOr(err + 1, bits);
 }
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// ---- mbarrier + bulk copy -----------------------------------------------------------------
+// ---- mbarriers, bulk copies, cluster -------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the cluster, with
+// release semantics at cluster scope (orders this thread's earlier stores into that CTA).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t local_bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait (about 2 s at the maximum SM clock, counted with the SM's cycle counter).
+constexpr long long kWaitLimitCycles = 4000000000ll;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long c0 = clock64();
   while (true) {
-    for (int i = 0; i < 32; ++i)
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > kWaitLimitCycles) return false;
   }
 }
-// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to shared memory;
-// completion is counted on `bar` as transaction bytes.
+// The same wait in every lane of a warp, with one warp-wide verdict.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to this CTA's
+// shared memory; completion is counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-// ---------------------------------------------------------------------------------------
-// Shrink.  A unit is (segment, up to 8 tokens, 8 rank columns); warp w computes column j0 + w:
-// its A page streams through registers in rounds of 8 x 16-byte loads per lane (4 KB per warp
-// in flight), each token row of the unit is read at the same positions, and one warp
-// reduction per token finishes each dot product.  No shared-memory staging and no barrier
-// inside a unit, so every resident warp keeps loads in flight.
-// ---------------------------------------------------------------------------------------
-constexpr int kShrinkThreads = 256;
-constexpr int TB = kShrinkTokBlock, RG = kShrinkRankGroup;
-constexpr int kShrinkRound = 8;                 // 16-byte vectors per lane per round
-
-__device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
-  float af[8], bf[8];
-  bf16x8_to_f32(a, af);
-  bf16x8_to_f32(b, bf);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc = fmaf(af[e], bf[e], acc);
-  return acc;
+// ---- warp-level MMA --------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D[16x8] += A[16x16] B[16x8], bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(kShrinkThreads, 2)
-shrink_kernel(LoraLaunch L, lora_segments seg) {
-  __shared__ int32_t sh_tok[TB];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait_then_release();
-  const int n_work = *seg.n_shrink;
-  const int H = L.H;
-  const int n_vec = H / 8;                      // 16-byte vectors per page
-
-  for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
-    const int s = seg.shrink_work[4 * w], tb = seg.shrink_work[4 * w + 1], g = seg.shrink_work[4 * w + 2];
-    const int a = seg.seg_adapter[s];
-    const int r = L.rank[a];
-    const int32_t* tab = L.ptab + ((int64_t)a * L.n_slots + L.slot) * kTabStride;   // [0][j]: A pages
-    const int t_begin = seg.seg_off[s] + tb * TB;
-    const int n_tok = min(TB, seg.seg_off[s + 1] - t_begin);
-    const int j = g * RG + warp;
-    __syncthreads();                            // previous unit done with sh_tok
-    if (tid < TB) sh_tok[tid] = tid < n_tok ? seg.perm[t_begin + tid] : 0;
-    __syncthreads();
-    if (tab[0] < 0 || j >= r) continue;         // no LoRA on this slot / column beyond the rank
-    const int64_t pg = tab[j];
-    if (pg < 0 || pg >= L.num_pages) {
-      if (lane == 0) flag_error(L.err, LORA_DEV_BAD_PAGE);
-      continue;
-    }
-    const uint4* A = reinterpret_cast<const uint4*>(L.pool + pg * H);
-    float acc[TB];
+// One work unit as the segment builder wrote it, plus the per-lane entries a warp gathers for
+// it: the page ids of rank columns lane and lane + 32 (-1 past the rank) and perm entries.
+struct Unit {
+  int r, t_begin, n_tok;
+  const int32_t* tab;
+};
+__device__ __forceinline__ int4 load_rec(const lora_segments& seg, int u, int n_units) {
+  return u < n_units ? __ldg(reinterpret_cast<const int4*>(seg.units) + u) : make_int4(0, 0, 0, 0);
+}
+__device__ __forceinline__ Unit unit_of(const LoraLaunch& L, const int4& rec) {
+  Unit U;
+  U.r = rec.y;
+  U.t_begin = rec.z;
+  U.n_tok = rec.w;
+  U.tab = L.ptab + ((int64_t)rec.x * L.n_slots + L.slot) * kTabStride;
+  return U;
+}
+struct Gathered {
+  int32_t pa[2], pb[2];
+  int32_t tok[4];
+};
+// Issue this lane's loads for unit U (values are consumed one unit later).  ntok_lane: how many
+// perm entries each lane reads; entry k of lane l is token tok_index(l, k) of the unit.
+template <int NTOK, typename F>
+__device__ __forceinline__ void gather_issue(const lora_segments& seg, const Unit& U, int lane, F tok_index,
+                                             Gathered& G) {
 #pragma unroll
-    for (int i = 0; i < TB; ++i) acc[i] = 0.f;
-    // Per round: the A vectors and the first token's row are loaded together; while a token's
-    // row is being multiplied, the next token's row is already in flight.
-    for (int base = 0; base < n_vec; base += 32 * kShrinkRound) {
-      uint4 av[kShrinkRound], xa[kShrinkRound], xb[kShrinkRound];
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    G.pa[h] = j < U.r ? __ldg(U.tab + j) : -1;
+    G.pb[h] = j < U.r ? __ldg(U.tab + LORA_MAX_RANK + j) : -1;
+  }
 #pragma unroll
-      for (int u = 0; u < kShrinkRound; ++u) {
-        const int v = base + u * 32 + lane;
-        av[u] = v < n_vec ? __ldg(A + v) : make_uint4(0, 0, 0, 0);
-        xa[u] = v < n_vec ? __ldg(reinterpret_cast<const uint4*>(L.x + (int64_t)sh_tok[0] * H) + v)
-                          : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < TB; i += 2) {
-        if (i + 1 < n_tok) {
-#pragma unroll
-          for (int u = 0; u < kShrinkRound; ++u) {
-            const int v = base + u * 32 + lane;
-            xb[u] = v < n_vec ? __ldg(reinterpret_cast<const uint4*>(L.x + (int64_t)sh_tok[i + 1] * H) + v)
-                              : make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (i < n_tok) {
-          float d = acc[i];
-#pragma unroll
-          for (int u = 0; u < kShrinkRound; ++u) d = dot8(av[u], xa[u], d);
-          acc[i] = d;
-        }
-        if (i + 2 < n_tok) {
-#pragma unroll
-          for (int u = 0; u < kShrinkRound; ++u) {
-            const int v = base + u * 32 + lane;
-            xa[u] = v < n_vec ? __ldg(reinterpret_cast<const uint4*>(L.x + (int64_t)sh_tok[i + 2] * H) + v)
-                              : make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (i + 1 < n_tok) {
-          float d = acc[i + 1];
-#pragma unroll
-          for (int u = 0; u < kShrinkRound; ++u) d = dot8(av[u], xb[u], d);
-          acc[i + 1] = d;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < TB; ++i) {
-      if (i < n_tok) {
-        float v = acc[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) seg.s[(int64_t)sh_tok[i] * LORA_MAX_RANK + j] = v;
-      }
-    }
+  for (int k = 0; k < NTOK; ++k) {
+    const int t = tok_index(lane, k);
+    G.tok[k] = t < U.n_tok ? __ldg(seg.perm + U.t_begin + t) : -1;
   }
 }
+__device__ __forceinline__ bool page_ok(int32_t p, int64_t num_pages) { return p >= 0 && p < num_pages; }
+// Bit j set when rank column j < r has both pages inside the pool (same value in every lane).
+__device__ __forceinline__ uint64_t valid_mask(const Gathered& G, int r, int64_t num_pages, int lane) {
+  uint64_t m = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const bool ok = lane + 32 * h < r && page_ok(G.pa[h], num_pages) && page_ok(G.pb[h], num_pages);
+    m |= (uint64_t)__ballot_sync(0xffffffffu, ok) << (32 * h);
+  }
+  return m;
+}
+__device__ __forceinline__ bool slot_has_lora(const Gathered& G) {
+  return __shfl_sync(0xffffffffu, G.pa[0], 0) >= 0;    // page table entry 0 of the slot
+}
+__device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_bar, uint32_t rank, const float (&v)[4]) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+               "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "r"(rb)
+               : "memory");
+}
 
-// ---------------------------------------------------------------------------------------
-// Expand.  A unit is (segment, up to 8 tokens, 1024 features); warp w owns 256 features, 8
-// per lane (one 16-byte slice of each B page).  Pages are read 8 at a time (8 loads per lane
-// in flight) and each slice is applied to all of the unit's tokens in the same pass, from
-// their s values in shared memory; the fp32 delta rows are written with 16-byte stores.
-// ---------------------------------------------------------------------------------------
-constexpr int kExpandThreads = 128;
-constexpr int kExpandFeat = 1024;
-constexpr int ETB = kExpandTokBlock;            // tokens per unit (8)
-constexpr int kExpandPages = 8;                 // pages in flight per lane
-
-__global__ void __launch_bounds__(kExpandThreads, 4)
-expand_kernel(LoraLaunch L, lora_segments seg) {
-  __shared__ float S[ETB][LORA_MAX_RANK];
-  __shared__ int64_t sh_page[LORA_MAX_RANK];
-  __shared__ int32_t sh_tok[ETB];
+__global__ void __launch_bounds__(kThreads, 1)
+lora_delta_kernel(LoraLaunch L, lora_segments seg) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait_then_release();
-  const int H = L.H;
-  const int n_fc = (H + kExpandFeat - 1) / kExpandFeat;
-  const int n_units = *seg.n_expand * n_fc;
+  const uint32_t q = cluster_rank();
+  const uint32_t ring = smem_u32(smem + kOffRing);
+  float* part = reinterpret_cast<float*>(smem + kOffPart);
+  float* exch = reinterpret_cast<float*>(smem + kOffExch);
+  __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smem + kOffSb);
+  const uint32_t bar_full = smem_u32(smem + kOffBar);
+  const uint32_t bar_empty = bar_full + 8 * kStages;
+  const uint32_t bar_exch = bar_empty + 8 * kStages;
 
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int w = u / n_fc, fc = u % n_fc;
-    const int s = seg.expand_work[2 * w], tg = seg.expand_work[2 * w + 1];
-    const int a = seg.seg_adapter[s];
-    const int r = L.rank[a];
-    const int32_t* tab = L.ptab + ((int64_t)a * L.n_slots + L.slot) * kTabStride + LORA_MAX_RANK;  // B pages
-    const int t_begin = seg.seg_off[s] + tg * ETB;
-    const int n_tok = min(ETB, seg.seg_off[s + 1] - t_begin);
-    __syncthreads();                            // previous unit done with the shared arrays
-    if (tab[0] < 0) continue;                   // no LoRA on this slot (uniform across the CTA)
-    if (tid < ETB) sh_tok[tid] = tid < n_tok ? seg.perm[t_begin + tid] : 0;
-    if (tid < LORA_MAX_RANK) {
-      int64_t pg = tid < r ? tab[tid] : -1;
-      if (tid < r && (pg < 0 || pg >= L.num_pages)) {
-        flag_error(L.err, LORA_DEV_BAD_PAGE);
-        pg = -1;
-      }
-      sh_page[tid] = pg;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
-    __syncthreads();
-    for (int i = tid; i < ETB * LORA_MAX_RANK; i += kExpandThreads) {
-      const int tk = i / LORA_MAX_RANK, j = i % LORA_MAX_RANK;
-      S[tk][j] = (tk < n_tok && j < r && sh_page[j] >= 0) ? seg.s[(int64_t)sh_tok[tk] * LORA_MAX_RANK + j] : 0.f;
-    }
-    __syncthreads();
-    const int f = fc * kExpandFeat + warp * 256 + lane * 8;
-    if (f >= H) continue;
-    {
-      constexpr int t0 = 0;
-      float acc[ETB][8];
+    for (int b = 0; b < 2; ++b) mbar_init(bar_exch + 8 * b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster_sync_all();                                     // peers' barriers exist before any remote access
+  pdl_wait_then_release();
+
+  const int H = L.H;
+  const int Hq = H / kCluster;                            // features per CTA (multiple of 16)
+  const int n_fb = (Hq + kFB - 1) / kFB;
+  const int f_cta = (int)q * Hq;
+  const int n_units = *seg.n_units;
+  const int n_groups = gridDim.x / kCluster;
+  const int group = blockIdx.x / kCluster;
+
+  if (warp == kConsumerWarps) {
+    // ================================ producer warp ================================
+    // Unit records and page ids are loaded one unit ahead, so their latency hides behind the
+    // copies of the current unit.
+    auto tok_lane = [](int l, int) { return l; };
+    uint32_t it = 0;
+    bool ok = true;
+    int4 rec = load_rec(seg, group, n_units);
+    Gathered G;
+    Unit U = unit_of(L, rec);
+    gather_issue<1>(seg, U, lane, tok_lane, G);
+    int4 rec_next = load_rec(seg, group + n_groups, n_units);
+    for (int u = group; u < n_units && ok; u += n_groups) {   // the producer alone may stop early
+      const Unit Un = unit_of(L, rec_next);
+      Gathered Gn;
+      gather_issue<1>(seg, Un, lane, tok_lane, Gn);
+      rec_next = load_rec(seg, u + 2 * n_groups, n_units);
+      if (slot_has_lora(G)) {
 #pragma unroll
-      for (int i = 0; i < ETB; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-      for (int j0 = 0; j0 < r; j0 += kExpandPages) {
-        uint4 bv[kExpandPages];
-#pragma unroll
-        for (int q = 0; q < kExpandPages; ++q) {
-          const int j = j0 + q;
-          const int64_t pg = j < r ? sh_page[j] : -1;
-          bv[q] = pg >= 0 ? __ldg(reinterpret_cast<const uint4*>(L.pool + pg * H + f)) : make_uint4(0, 0, 0, 0);
+        for (int h = 0; h < 2; ++h) {
+          if (lane + 32 * h < U.r && !(page_ok(G.pa[h], L.num_pages) && page_ok(G.pb[h], L.num_pages))) {
+            flag_error(L.err, LORA_DEV_BAD_PAGE);
+            G.pa[h] = G.pb[h] = -1;                       // the column is dropped on both sides
+          }
         }
-#pragma unroll
-        for (int q = 0; q < kExpandPages; ++q) {
-          float bf[8];
-          bf16x8_to_f32(bv[q], bf);
-          const int j = min(j0 + q, LORA_MAX_RANK - 1);   // S is zero past the rank
-#pragma unroll
-          for (int i = 0; i < ETB; ++i) {
-            const float sv = S[i][j];                    // zero for tokens past n_tok
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(sv, bf[e], acc[i][e]);
+        const int ng = (U.r + 15) / 16;
+        // stages in consumption order: per feature block, x then the A groups; then the B groups
+        for (int phase = 0; phase < 2 && ok; ++phase) {
+          for (int fb = 0; fb < n_fb && ok; ++fb) {
+            const int fw = min(kFB, Hq - fb * kFB);
+            const int f0 = f_cta + fb * kFB;
+            const uint32_t pitch = fw * 2 + 16;
+            for (int g = (phase == 0 ? -1 : 0); g < ng; ++g) {
+              const int s = it % kStages;
+              ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1));
+              if (!ok) break;
+              const uint16_t* src = nullptr;
+              if (g < 0) {                                 // x rows of the unit's tokens
+                if (lane < U.n_tok) src = L.x + (int64_t)G.tok[0] * H + f0;
+              } else {
+                const int32_t* pg = phase == 0 ? G.pa : G.pb;
+                const int32_t page = __shfl_sync(0xffffffffu, (g >> 1) ? pg[1] : pg[0], 16 * (g & 1) + (lane & 15));
+                if (lane < 16 && page >= 0) src = L.pool + (int64_t)page * H + f0;
+              }
+              const uint32_t rows = __popc(__ballot_sync(0xffffffffu, src != nullptr));
+              if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, rows * fw * 2);
+              __syncwarp();
+              if (src) bulk_g2s(ring + s * kSlotBytes + lane * pitch, src, fw * 2, bar_full + 8 * s);
+              ++it;
+            }
           }
         }
       }
+      U = Un;
+      G = Gn;
+    }
+    if (!ok) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
+    // Drain: the most recent use of every slot has landed before the CTA can exit.
+    if (lane == 0)
+      for (uint32_t k = it > (uint32_t)kStages ? it - kStages : 0; k < it; ++k)
+        if (!mbar_wait(bar_full + 8 * (k % kStages), (k / kStages) & 1)) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
+  } else {
+    // ================================ consumer warps ================================
+    // After a failed wait the warps keep walking the same sequence of units, stages and barriers
+    // (skipping the waits), so every named and cluster barrier still sees all its threads.
+    // Lane l stores delta for tokens tok_store(l, k), k < 4 (the MMA accumulator layout).
+    auto tok_store = [](int l, int k) { return (k >> 1) * 8 + 2 * (l & 3) + (k & 1); };
+    uint32_t it = 0, n_done = 0;
+    bool ok = true;
+    const int mi = lane >> 3, ri = lane & 7;              // ldmatrix: matrix and row this lane addresses
+    __nv_bfloat16* sb_hi = sb;
+    __nv_bfloat16* sb_lo = sb + kUnitTok * kSbPitch;
+    int4 rec = load_rec(seg, group, n_units);
+    Gathered G;
+    Unit U = unit_of(L, rec);
+    gather_issue<4>(seg, U, lane, tok_store, G);
+    int4 rec_next = load_rec(seg, group + n_groups, n_units);
+    for (int u = group; u < n_units; u += n_groups) {
+      const Unit Un = unit_of(L, rec_next);
+      Gathered Gn;
+      gather_issue<4>(seg, Un, lane, tok_store, Gn);
+      rec_next = load_rec(seg, u + 2 * n_groups, n_units);
+      if (slot_has_lora(G)) {
+        const uint64_t vm = valid_mask(G, U.r, L.num_pages, lane);
+        const int ng = (U.r + 15) / 16;
+        const int wpg = kConsumerWarps / ng;              // warps per page group in the shrink
+        const int my_g = warp / wpg, sub = warp % wpg;
+
+        // ---- shrink over this CTA's feature quarter: acc[n-tile] = A_g^T x^T (16 pages x 8 tokens)
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int fb = 0; fb < n_fb; ++fb) {
+          const int fw = min(kFB, Hq - fb * kFB);
+          const uint32_t pitch = fw * 2 + 16;
+          const int sx = it % kStages;
+          ok = ok && wait_warp(bar_full + 8 * sx, (it / kStages) & 1);
+          ++it;
+          const uint32_t xbase = ring + sx * kSlotBytes;
+          for (int g = 0; g < ng; ++g) {
+            const int s = it % kStages;
+            ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
+            ++it;
+            if (ok && g == my_g) {
+              const uint32_t abase = ring + s * kSlotBytes;
+              const uint32_t a_row = abase + (ri + 8 * (mi & 1)) * pitch + 16 * (mi >> 1);
+              const uint32_t x_row = xbase + (ri + 8 * (mi >> 1)) * pitch + 16 * (mi & 1);
+#pragma unroll 4
+              for (int ks = sub; ks < fw / 16; ks += wpg) {
+                uint32_t af[4], xf[4];
+                ldsm_x4(a_row + ks * 32, af);
+                ldsm_x4(x_row + ks * 32, xf);
+                mma_bf16(acc[0], af, xf[0], xf[1]);
+                mma_bf16(acc[1], af, xf[2], xf[3]);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + 8 * sx);
+        }
+        // partial sums of this warp: part[warp][page][token]
+        if (my_g < ng) {
+          float* pw = part + warp * 256;
 #pragma unroll
-      for (int i = 0; i < ETB; ++i) {
-        if (t0 + i < n_tok) {
-          float4* dst = reinterpret_cast<float4*>(L.delta + (int64_t)sh_tok[t0 + i] * H + f);
-          dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-          dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+          for (int nt = 0; nt < 2; ++nt) {
+            const int m = lane >> 2, n = nt * 8 + 2 * (lane & 3);
+            pw[m * 16 + n] = acc[nt][0];
+            pw[m * 16 + n + 1] = acc[nt][1];
+            pw[(m + 8) * 16 + n] = acc[nt][2];
+            pw[(m + 8) * 16 + n + 1] = acc[nt][3];
+          }
+        }
+        consumer_sync();
+        // This CTA's partial of s over its quarter goes to all four CTAs, exch[b][q][j][t], as
+        // asynchronous remote stores that count their bytes on the receiver's barrier.
+        const int b = n_done & 1;
+        if (tid == 0) mbar_arrive_expect_tx(bar_exch + 8 * b, kCluster * ng * 256 * 4);
+        if (tid < ng * 64) {
+          const int j = tid >> 2, t0 = (tid & 3) * 4, g = j >> 4;
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float acc_v = 0.f;
+            for (int k = 0; k < wpg; ++k) acc_v += part[(g * wpg + k) * 256 + (j & 15) * 16 + t0 + i];
+            v[i] = (((vm >> j) & 1) && t0 + i < U.n_tok) ? acc_v : 0.f;
+          }
+          const uint32_t dst = smem_u32(exch + ((b * kCluster + q) * LORA_MAX_RANK + j) * kUnitTok + t0);
+#pragma unroll
+          for (int c = 0; c < kCluster; ++c) st_async_v4(dst, bar_exch + 8 * b, (uint32_t)c, v);
+        }
+        ok = ok && wait_warp(bar_exch + 8 * b, (n_done >> 1) & 1);
+        ++n_done;
+        // s = sum of the four quarters (fixed order), split into bf16 hi + lo, token-major
+        for (int e = tid; e < ng * 256; e += kConsumers) {
+          const int j = e >> 4, t = e & 15;
+          const float* ex = exch + (b * kCluster * LORA_MAX_RANK + j) * kUnitTok + t;
+          const float v = ((ex[0] + ex[LORA_MAX_RANK * kUnitTok]) + ex[2 * LORA_MAX_RANK * kUnitTok]) +
+                          ex[3 * LORA_MAX_RANK * kUnitTok];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+          sb_hi[t * kSbPitch + j] = hi;
+          sb_lo[t * kSbPitch + j] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        }
+        consumer_sync();
+
+        // ---- expand: delta[t][f] for this CTA's features, warp w owns 128 features per block
+        for (int fb = 0; fb < n_fb; ++fb) {
+          const int fw = min(kFB, Hq - fb * kFB);
+          const uint32_t pitch = fw * 2 + 16;
+          const int f_warp = warp * 128;
+          float e[8][2][4];
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) e[mt][nt][k] = 0.f;
+          for (int g = 0; g < ng; ++g) {
+            const int s = it % kStages;
+            ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
+            ++it;
+            if (ok && f_warp < fw) {
+              uint32_t sh[4], sl[4];
+              const uint32_t s_off = ((ri + 8 * (mi >> 1)) * kSbPitch + 16 * g + 8 * (mi & 1)) * 2;
+              ldsm_x4(smem_u32(sb_hi) + s_off, sh);
+              ldsm_x4(smem_u32(sb_lo) + s_off, sl);
+              // A-fragment elements of page columns without valid pages are zeroed
+              const uint32_t kb = 16 * g + 2 * (lane & 3);
+              const uint32_t m01 = (((vm >> kb) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 1)) & 1) ? 0xFFFF0000u : 0u);
+              const uint32_t m23 = (((vm >> (kb + 8)) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 9)) & 1) ? 0xFFFF0000u : 0u);
+              const uint32_t b_row = ring + s * kSlotBytes + (ri + 8 * (mi >> 1)) * pitch + 16 * (mi & 1);
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt) {
+                if (f_warp + mt * 16 < fw) {
+                  uint32_t af[4];
+                  ldsm_x4_t(b_row + (f_warp + mt * 16) * 2, af);
+                  af[0] &= m01;
+                  af[1] &= m01;
+                  af[2] &= m23;
+                  af[3] &= m23;
+                  mma_bf16(e[mt][0], af, sh[0], sh[1]);
+                  mma_bf16(e[mt][0], af, sl[0], sl[1]);
+                  mma_bf16(e[mt][1], af, sh[2], sh[3]);
+                  mma_bf16(e[mt][1], af, sl[2], sl[3]);
+                }
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+          }
+          if (!ok) continue;
+          // store the valid tokens' rows of delta
+          const int fbase = f_cta + fb * kFB + f_warp + (lane >> 2);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            if (f_warp + mt * 16 < fw) {
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int tk = G.tok[nt * 2 + (k & 1)];
+                  if (tk >= 0) L.delta[(int64_t)tk * H + fbase + mt * 16 + 8 * (k >> 1)] = e[mt][nt][k];
+                }
+            }
+          }
         }
       }
+      U = Un;
+      G = Gn;
     }
+    if (!ok && lane == 0) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
   }
+  cluster_sync_all();                                     // no CTA leaves while a peer may still address it
 }
 
-inline int grid_cap(int upper, int cap) { return upper < cap ? (upper > 0 ? upper : 1) : cap; }
+int active_clusters() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster * 64);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, lora_delta_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = device_sm_count() / kCluster;
+  }
+  cached[dev] = n;
+  return n;
+}
 
 }  // namespace
 
-// Grids loop over the work list (its length is only known on the device), capped at what
-// stays resident: two shrink CTAs (8 warps each) and four expand CTAs (4 warps each) per SM.
-int launch_shrink(const LoraLaunch& L, cudaStream_t st) {
-  const int grid = grid_cap(L.seg->shrink_cap, device_sm_count() * 2);
-  cudaError_t e = launch_pdl(L.pdl, shrink_kernel, dim3(grid), dim3(kShrinkThreads), 0, st, L, *L.seg);
+int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(lora_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return lora_cuda_fail(e, "lora_delta_kernel: shared memory attribute");
+    attr_set[dev] = true;
+  }
+  // Persistent clusters, as many as can be resident; each loops over the units.
+  int groups = active_clusters();
+  if (L.seg->unit_cap < groups) groups = L.seg->unit_cap > 0 ? L.seg->unit_cap : 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * kCluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = kCluster;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = L.pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_delta_kernel, L, *L.seg);
   if (e == cudaSuccess) e = cudaGetLastError();
-  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "shrink_kernel launch");
-}
-
-int launch_expand(const LoraLaunch& L, cudaStream_t st) {
-  const int n_fc = (L.H + kExpandFeat - 1) / kExpandFeat;
-  const int grid = grid_cap(L.seg->expand_cap * n_fc, device_sm_count() * 4);
-  cudaError_t e = launch_pdl(L.pdl, expand_kernel, dim3(grid), dim3(kExpandThreads), 0, st, L, *L.seg);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "expand_kernel launch");
+  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "lora_delta_kernel launch");
 }

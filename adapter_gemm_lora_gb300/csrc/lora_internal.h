@@ -48,7 +48,7 @@ struct lora_pool {
   std::vector<uint16_t> h_stage;
 
   // kernel accounting (lora_profile_*)
-  int64_t launches[LORA_N_KINDS] = {0, 0, 0, 0, 0};
+  int64_t launches[LORA_N_KINDS] = {0, 0, 0, 0};
   bool prof_on = false;
   struct ProfRec { int kind; cudaEvent_t start, stop; };
   std::vector<ProfRec> prof_rec;
@@ -88,8 +88,7 @@ struct LoraLaunch {
   int32_t* err;
   bool pdl;
 };
-int launch_shrink(const LoraLaunch& L, cudaStream_t st);
-int launch_expand(const LoraLaunch& L, cudaStream_t st);
+int launch_lora_delta(const LoraLaunch& L, cudaStream_t st);
 
 struct GemmLaunch {
   const uint16_t* x;       // [T][H]
@@ -135,6 +134,4 @@ inline cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim
 int device_sm_count();
 
 // Work-list geometry shared by the segment builder and the gather kernels.
-constexpr int kShrinkTokBlock = 8;   // tokens per shrink unit
-constexpr int kShrinkRankGroup = 8;  // rank columns per shrink unit
-constexpr int kExpandTokBlock = 8;   // tokens per expand unit
+constexpr int kUnitTokens = 16;      // tokens per LoRA-delta work unit

@@ -117,7 +117,7 @@ int lora_profile_enable(lora_pool* p, int32_t enable) {
 
 int lora_profile_read(lora_pool* p, int32_t n_kinds, int64_t* launches, double* ms, int32_t reset) {
   if (!p || n_kinds < 0 || (n_kinds > 0 && (!launches || !ms))) return lora_fail(LORA_EINVAL, "lora_profile_read: bad arguments");
-  double acc[LORA_N_KINDS] = {0, 0, 0, 0, 0};
+  double acc[LORA_N_KINDS] = {0, 0, 0, 0};
   int rc = LORA_OK;
   for (auto& r : p->prof_rec) {
     float t = 0.f;
@@ -411,14 +411,13 @@ int lora_status(lora_pool* p, lora_stream_t stream) {
 // ---- segment workspace -----------------------------------------------------------------
 namespace {
 struct SegLayout {
-  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, shrink_work, n_shrink, expand_work, n_expand, s, delta, total;
-  int32_t max_seg, shrink_cap, expand_cap;
+  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, total;
+  int32_t max_seg, unit_cap;
 };
 SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
   SegLayout L{};
   L.max_seg = std::min<int32_t>(T_max, p->max_adapters);
-  L.expand_cap = T_max / kExpandTokBlock + L.max_seg + 1;
-  L.shrink_cap = (T_max / kShrinkTokBlock + L.max_seg + 1) * (LORA_MAX_RANK / kShrinkRankGroup);
+  L.unit_cap = T_max / kUnitTokens + L.max_seg + 1;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   L.perm = take((size_t)T_max * 4);
@@ -426,11 +425,8 @@ SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
   L.seg_adapter = take((size_t)(L.max_seg + 1) * 4);
   L.n_seg = take(16);
   L.tok_adapter = take((size_t)T_max * 4);
-  L.shrink_work = take((size_t)L.shrink_cap * 16);
-  L.n_shrink = take(16);
-  L.expand_work = take((size_t)L.expand_cap * 8);
-  L.n_expand = take(16);
-  L.s = take((size_t)T_max * LORA_MAX_RANK * 4);
+  L.units = take((size_t)L.unit_cap * 16);
+  L.n_units = take(16);
   L.delta = take((size_t)T_max * p->H * 4);
   L.total = off;
   return L;
@@ -461,13 +457,10 @@ int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T
   seg->seg_adapter = reinterpret_cast<int32_t*>(b + L.seg_adapter);
   seg->n_seg = reinterpret_cast<int32_t*>(b + L.n_seg);
   seg->tok_adapter = reinterpret_cast<int32_t*>(b + L.tok_adapter);
-  seg->shrink_work = reinterpret_cast<int32_t*>(b + L.shrink_work);
-  seg->n_shrink = reinterpret_cast<int32_t*>(b + L.n_shrink);
-  seg->expand_work = reinterpret_cast<int32_t*>(b + L.expand_work);
-  seg->n_expand = reinterpret_cast<int32_t*>(b + L.n_expand);
-  seg->shrink_cap = L.shrink_cap;
-  seg->expand_cap = L.expand_cap;
-  seg->s = reinterpret_cast<float*>(b + L.s);
+  seg->units = reinterpret_cast<int32_t*>(b + L.units);
+  seg->n_units = reinterpret_cast<int32_t*>(b + L.n_units);
+  seg->unit_cap = L.unit_cap;
+  seg->reserved = 0;
   seg->delta = reinterpret_cast<float*>(b + L.delta);
   return LORA_OK;
 }

@@ -8,8 +8,9 @@
 //
 // One CTA of 1024 threads: a shared-memory histogram over adapter ids (with each used
 // adapter's rank), one block scan that turns counts into run starts, segment indices and the
-// offsets of the shrink and expand work lists (written right away), then a stable scatter in
-// chunks of 1024 tokens (warp-level match for ranks inside a warp, warps in order).
+// offsets of the LoRA-delta work units (each written right away as a complete record:
+// adapter, rank, first index into perm, token count), then a stable scatter in chunks of
+// 1024 tokens (warp-level match for ranks inside a warp, warps in order).
 #include <cuda_runtime.h>
 
 #include "lora_internal.h"
@@ -100,16 +101,13 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   //    writes the segments and work units of its own keys
   const int per = (K + kThreads - 1) / kThreads;
   const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
-  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, expand units, shrink units
+  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, work units, -
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     v[0] += c;
     if (k > 0 && c > 0) {
-      const int32_t nb_e = (c + kExpandTokBlock - 1) / kExpandTokBlock;
-      const int32_t nb_s = (c + kShrinkTokBlock - 1) / kShrinkTokBlock;
       v[1] += 1;
-      v[2] += nb_e;
-      v[3] += nb_s * ((krank[k] + kShrinkRankGroup - 1) / kShrinkRankGroup);
+      v[2] += (c + kUnitTokens - 1) / kUnitTokens;
     }
   }
   int32_t tot[4];
@@ -120,20 +118,9 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
       const int32_t sidx = v[1];
       seg.seg_off[sidx] = v[0];
       seg.seg_adapter[sidx] = k - 1;
-      const int32_t nb_e = (c + kExpandTokBlock - 1) / kExpandTokBlock;
-      for (int b = 0; b < nb_e; ++b, ++v[2]) {
-        seg.expand_work[2 * v[2]] = sidx;
-        seg.expand_work[2 * v[2] + 1] = b;
-      }
-      const int32_t nb_s = (c + kShrinkTokBlock - 1) / kShrinkTokBlock;
-      const int32_t ng = (krank[k] + kShrinkRankGroup - 1) / kShrinkRankGroup;
-      for (int b = 0; b < nb_s; ++b)
-        for (int gi = 0; gi < ng; ++gi, ++v[3]) {
-          seg.shrink_work[4 * v[3]] = sidx;
-          seg.shrink_work[4 * v[3] + 1] = b;
-          seg.shrink_work[4 * v[3] + 2] = gi;
-          seg.shrink_work[4 * v[3] + 3] = 0;
-        }
+      for (int b = 0; b * kUnitTokens < c; ++b, ++v[2])
+        reinterpret_cast<int4*>(seg.units)[v[2]] =
+            make_int4(k - 1, krank[k], v[0] + b * kUnitTokens, min(kUnitTokens, c - b * kUnitTokens));
       ++v[1];
     }
     cnt[k] = v[0];                             // becomes the running write position of key k
@@ -144,8 +131,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
     seg.seg_off[S] = T;
     if (S == 0) seg.seg_off[0] = T;
     *seg.n_seg = S;
-    *seg.n_expand = tot[2];
-    *seg.n_shrink = tot[3];
+    *seg.n_units = tot[2];
   }
   __syncthreads();
 

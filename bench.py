@@ -2,8 +2,8 @@
 """Benchmark: tokens/s through the batched multi-LoRA projections, and roofline fraction.
 
 One step = one pass of the whole hot path over one batch: the segment build (tokens grouped
-by adapter) plus lora_linear_forward on every projection slot of the workload (paged shrink,
-paged expand, tcgen05 base GEMM with the fused delta epilogue).  Adapters are resident
+by adapter) plus lora_linear_forward on every projection slot of the workload (LoRA delta:
+paged shrink and expand fused; tcgen05 base GEMM with the fused delta epilogue).  Adapters are resident
 (loading is set-up, not timed).  Default workload: the decode batch (H=4096, q/k/v/o,
 256 requests x 1 token, 64 adapters of rank 8..64, Zipf(1.0) request->adapter, pool of
 2^18 pages half filled with KV pages).  Other workloads with --config 1..5.

@@ -77,9 +77,12 @@ typedef struct lora_pool_stats_t {
  *                    the number of no-adapter tokens and seg_off[S] = T;
  *   seg_adapter[S]   adapter id of segment s, ascending;
  *   n_seg[1]         S;
- * plus work lists and fp32 scratch (the shrink output s and the LoRA delta) used by
- * lora_linear_forward.  Calls that use the same workspace must be ordered on one
- * stream: the scratch is reused by every projection slot.
+ *   units[4 U]       LoRA-delta work units, U = *n_units: unit u covers the tokens
+ *                    perm[units[4u+2] .. units[4u+2] + units[4u+3]) (at most 16, all of one
+ *                    segment) of adapter units[4u], whose rank is units[4u+1];
+ * plus the fp32 scratch for the LoRA delta used by lora_linear_forward.  Calls that use
+ * the same workspace must be ordered on one stream: the scratch is reused by every
+ * projection slot.
  */
 typedef struct lora_segments {
   int32_t T_max;          /* token capacity of the workspace */
@@ -91,13 +94,10 @@ typedef struct lora_segments {
   int32_t* seg_adapter;
   int32_t* n_seg;
   int32_t* tok_adapter;   /* [T_max] validated adapter id per token (-1 = none or rejected) */
-  int32_t* shrink_work;   /* [4 * shrink_cap] (segment, token block, rank group, -) */
-  int32_t* n_shrink;
-  int32_t* expand_work;   /* [2 * expand_cap] (segment, token block) */
-  int32_t* n_expand;
-  int32_t shrink_cap;
-  int32_t expand_cap;
-  float*   s;             /* [T_max][64] x_t A for the token's adapter (fp32) */
+  int32_t* units;         /* [4 * unit_cap] (adapter, rank, first perm index, tokens) */
+  int32_t* n_units;
+  int32_t unit_cap;
+  int32_t reserved;
   float*   delta;         /* [T_max][H]  (x_t A) B (fp32) */
 } lora_segments;
 
@@ -176,8 +176,8 @@ int lora_segments_build(lora_pool* pool, const int32_t* token_adapter, int32_t T
  *   y      device bf16 [T][H] row-major, written (out of place; must not alias x);
  *   delta_dbg  nullable device fp32 [T][H]: receives the LoRA term alone (0 for tokens
  *          without LoRA on this slot), for parity tests.
- * Kernels: paged shrink (s), paged expand (delta), tcgen05 base GEMM with an epilogue that
- * adds the delta before the single bf16 rounding.
+ * Kernels: the LoRA delta (paged shrink and expand fused, s kept on chip), then the tcgen05
+ * base GEMM with an epilogue that adds the delta before the single bf16 rounding.
  * Errors: LORA_EINVAL (slot, pointers, no batch built), LORA_ECUDA (launch failure).
  */
 int lora_linear_forward(lora_pool* pool, const lora_segments* seg, int32_t slot,
@@ -197,7 +197,8 @@ const char* lora_last_error(void);
 
 /*
  * Kernel accounting for benchmarks.  Every kernel this library launches for `pool` is counted
- * by kind: 0 segment build, 1 shrink, 2 expand, 3 base GEMM, 4 page scatter (adapter loads).
+ * by kind: 0 segment build, 1 LoRA delta (shrink and expand), 2 base GEMM, 3 page scatter
+ * (adapter loads).
  * With profiling enabled, each launch is also bracketed by CUDA events recorded on the
  * stream it runs on (also inside a stream capture: the events then become graph nodes and
  * are re-recorded by every replay).  lora_profile_read synchronises those events and
@@ -206,11 +207,10 @@ const char* lora_last_error(void);
  * Events cost ~1 us of host time per launch.
  */
 #define LORA_KIND_SEGMENTS 0
-#define LORA_KIND_SHRINK   1
-#define LORA_KIND_EXPAND   2
-#define LORA_KIND_GEMM     3
-#define LORA_KIND_SCATTER  4
-#define LORA_N_KINDS       5
+#define LORA_KIND_DELTA    1
+#define LORA_KIND_GEMM     2
+#define LORA_KIND_SCATTER  3
+#define LORA_N_KINDS       4
 int lora_profile_enable(lora_pool* pool, int32_t enable);
 int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, double* ms_host,
                       int32_t reset);
