@@ -54,7 +54,7 @@ class lora_segments(ctypes.Structure):
                 ("perm", ctypes.c_void_p), ("seg_off", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
                 ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("units", ctypes.c_void_p),
                 ("n_units", ctypes.c_void_p), ("unit_cap", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("delta", ctypes.c_void_p)]
+                ("delta", ctypes.c_void_p), ("gemm_partials", ctypes.c_void_p)]
 
 
 class lora_pool_stats_t(ctypes.Structure):

@@ -62,6 +62,8 @@ extern "C" int lora_linear_forward(lora_pool* p, const lora_segments* seg, int32
   G.H = H;
   G.slot = slot;
   G.n_slots = p->n_slots;
+  G.partials = seg->gemm_partials;
+  G.partials_floats = gemm_partial_floats(seg->T_max, H);
   G.err = p->d_err;
   G.pdl = !p->prof_on;
   ProfScope prof(p, LORA_KIND_GEMM, st);

@@ -51,10 +51,11 @@ constexpr int THREADS = 256;
 struct GemmParams {
   uint16_t* y;
   const float* delta;
+  float* partials;
   const int32_t* tok_adapter;
   const int32_t* ptab;
   int32_t* err;
-  int32_t T, H, BN, n_kb, kc, stages, cn, slot, n_slots;
+  int32_t T, H, BN, n_kb, kc, stages, cn, ks, slot, n_slots;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -129,14 +130,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int
                "r"(c0), "r"(c1), "r"(src)
                : "memory");
 }
-__device__ __forceinline__ void bulk_commit_and_wait_all() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -152,21 +146,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 
 // ---- tcgen05 ----------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -248,6 +227,121 @@ __host__ __device__ inline uint32_t tmem_cols_for(int bn) {
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
+// Ballot masks of the tokens (columns) that carry LoRA on this slot, for the 32-column chunks
+// c0, c0 + step, ... (at most 4): all id loads are issued before any page-table load, so the two
+// dependent global reads cost one latency each for every chunk of the warp together.
+__device__ __forceinline__ void presence_masks(const GemmParams& p, int t_col0, int c0, int step, int c_end, int lane,
+                                               unsigned (&pm)[4]) {
+  int a[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = c0 + k * step;
+    const int tl = t_col0 + c * 32 + lane;
+    a[k] = (c < c_end && tl < p.T) ? p.tok_adapter[tl] : -1;
+  }
+  int present[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    present[k] = a[k] >= 0 ? p.ptab[((int64_t)a[k] * p.n_slots + p.slot) * kTabStride] >= 0 : 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) pm[k] = __ballot_sync(0xffffffffu, present[k]);
+}
+
+__device__ __forceinline__ void bulk_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Epilogue when K is split over a cluster of ks CTAs (one token tile of BN columns).  CTA `me`
+// owns token columns [me*w, (me+1)*w), w = BN/ks.  Every CTA writes the fp32 partial sums of
+// the other owners' columns from TMEM to a global scratch block (coalesced, stays in L2); after
+// a cluster barrier each owner reads the ks-1 blocks of its columns, adds the ks partials in
+// cluster-rank order (the same order in every CTA), adds the delta and writes its columns of y
+// straight from registers.  Scratch block of (owner o, sender s): [w tokens][128 features] at
+// index (m_tile * ks + o) * (ks - 1) + (s < o ? s : s - 1).
+template <int KS>
+__device__ __forceinline__ void split_k_epilogue(const GemmParams& p, uint32_t tmem_row, int m0, int t0, int me, int row,
+                                                 int lane, int h, bool ok) {
+  constexpr int ks = KS;
+  const int w = p.BN / ks;
+  const int m_tile = m0 / BM;
+  const int feat = m0 + row;                      // this thread's output feature
+  const size_t blk = (size_t)w * BM;
+  // The scratch was last read by the GEMM launch before this one, and the delta and ids come
+  // from the kernels before this one: wait for them before writing or reading.
+  pdl_wait_then_release();
+  if (ok) {
+    for (int c = h; c < p.BN / 32; c += 2) {      // other owners' columns: this CTA's partials
+      const int o = (c * 32) / w;
+      if (o == me) continue;
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
+      tmem_ld_wait();
+      float* dst = p.partials + (size_t)((m_tile * ks + o) * (ks - 1) + (me < o ? me : me - 1)) * blk +
+                   (size_t)(c * 32 - o * w) * BM + row;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[(size_t)i * BM] = __uint_as_float(v[i]);
+    }
+  }
+  __threadfence();                                // this thread's partials are visible GPU-wide
+  // Loads for the first own chunk go out before the barrier and stay in flight across it: the
+  // delta column block (selected by the presence mask later) and the presence lookups.
+  const int c_first = me * (w / 32) + h, c_end = (me + 1) * (w / 32);
+  float dv[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int t = t0 + c_first * 32 + i;
+    dv[i] = (c_first < c_end && t < p.T && feat < p.H) ? __ldg(p.delta + (size_t)t * p.H + feat) : 0.f;
+  }
+  unsigned pm[4];                                 // own chunks c_first + 2k
+  presence_masks(p, t0, c_first, 2, c_end, lane, pm);
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // all partials of the cluster
+  if (!ok) return;
+#pragma unroll 1
+  for (int k = 0; k < 4; ++k) {                   // own columns
+    const int c = c_first + 2 * k;
+    if (c >= c_end) break;
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
+    tmem_ld_wait();
+    const unsigned pmask = k == 0 ? pm[0] : k == 1 ? pm[1] : k == 2 ? pm[2] : pm[3];
+    const size_t off0 = (size_t)(c * 32 - me * w) * BM + row;
+    const float* in0 = p.partials + (size_t)(m_tile * ks + me) * (ks - 1) * blk + off0;
+    const int tc = t0 + c * 32;
+    if (k > 0) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        dv[i] = (tc + i < p.T && feat < p.H) ? __ldg(p.delta + (size_t)(tc + i) * p.H + feat) : 0.f;
+    }
+    // the ks-1 peer partials of this chunk, all loads in flight together
+    float pv[ks - 1][32];
+#pragma unroll
+    for (int j = 0; j < ks - 1; ++j)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pv[j][i] = __ldcg(in0 + (size_t)j * blk + (size_t)i * BM);
+    // acc = partial of rank 0, then + rank 1, + rank 2, ... (peer slot of rank s: s, or s-1 past me)
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = me == 0 ? __uint_as_float(v[i]) : pv[0][i];
+#pragma unroll
+    for (int src = 1; src < ks; ++src) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float peer = src < me ? pv[src < ks - 1 ? src : ks - 2][i] : pv[src - 1][i];
+        acc[i] += src == me ? __uint_as_float(v[i]) : peer;
+      }
+    }
+    if (feat < p.H) {
+      // all loads of the chunk precede its first y store: the compiler cannot rule out that y
+      // aliases them, and would otherwise wait out each load in turn
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (tc + i < p.T) p.y[(size_t)(tc + i) * p.H + feat] = f32_to_bf16_rn((pmask >> i) & 1u ? acc[i] + dv[i] : acc[i]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_y, GemmParams p) {
@@ -263,13 +357,16 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int m0 = blockIdx.y * BM;
   const int t0 = blockIdx.z * p.BN;
   const int cn = p.cn;                                  // CTAs sharing the W tile (cluster along tokens)
+  const int ks = p.ks;                                  // CTAs splitting K (cluster along x); cn == 1 then
   const uint32_t crank = cn > 1 ? cluster_ctarank() : 0;
+  const int me = ks > 1 ? (int)cluster_ctarank() : 0;   // this CTA's K slice
+  const int kb0 = me * (p.n_kb / ks);                   // first 64-wide K block of the slice
   const uint16_t cmask = (uint16_t)((1u << cn) - 1u);
   const int stages = p.stages;
   const int kc = p.kc;                                  // 64-wide K chunks per stage
   const uint32_t xb = (uint32_t)(p.BN * BK * 2);        // one x chunk
   const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
-  const int nk = p.n_kb / kc;                           // stages' worth of K (n_kb is a multiple of kc)
+  const int nk = p.n_kb / ks / kc;                      // stages' worth of K in this CTA's slice
   const uint32_t ncols = tmem_cols_for(p.BN);
 
   if (threadIdx.x == 0) {
@@ -292,7 +389,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (cn > 1) cluster_sync_all();                       // peers' barriers exist before anything targets them
+  if (cn > 1 || ks > 1) cluster_sync_all();             // peers' barriers exist before anything targets them
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
@@ -313,7 +410,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         mbar_arrive_expect_tx(bar_full + 8 * s, tx);
         const uint32_t st = s_base + (uint32_t)s * stage_bytes;
         for (int c = 0; c < kc; ++c) {
-          const int kx = (i * kc + c) * BK;
+          const int kx = (kb0 + i * kc + c) * BK;
           const uint32_t wdst = st + (uint32_t)c * A_BYTES;
           if (cn > 1)
             tma_load_2d_multicast(wdst + crank * (uint32_t)(w_rows * BK * 2), &tm_w, kx, m0 + (int)crank * w_rows,
@@ -359,43 +456,54 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (!ok && lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
   ok = __syncthreads_and(ok) != 0;
   tc_fence_after();
-  pdl_wait_then_release();         // the delta and validated ids come from the kernels before this one
   const int q = warp & 3, h = warp >> 2;
   const int row = q * 32 + lane;
+  const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+  if (ks > 1) {
+    if (ks == 4)
+      split_k_epilogue<4>(p, tmem_row, m0, t0, me, row, lane, h, ok);
+    else
+      split_k_epilogue<2>(p, tmem_row, m0, t0, me, row, lane, h, ok);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, ncols);
+    cluster_sync_all();                           // no peer may still write into this CTA
+    return;
+  }
+  pdl_wait_then_release();         // the delta and validated ids come from the kernels before this one
   // Stage memory is free now (every multicast into it belonged to a k-block consumed above):
   // the fp32 delta tile [BN][128] at 0, the bf16 output tile [BN][128] after it (<= 192 KB).
   const uint32_t delta_s = s_base;
   const uint32_t y_s = s_base + (uint32_t)(p.BN * BM * 4);
-  const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+  const float* delta_p = reinterpret_cast<const float*>(smem);
+  uint16_t* y_p = reinterpret_cast<uint16_t*>(smem + (size_t)p.BN * BM * 4);
   if (threadIdx.x == 0 && ok) {
     mbar_arrive_expect_tx(bar_delta, (uint32_t)(p.BN * BM * 4));
     tma_load_2d_plain(delta_s, &tm_d, m0, t0, bar_delta);
   }
+  unsigned pm[4];                                 // chunks h + 2k
+  presence_masks(p, t0, h, 2, p.BN / 32, lane, pm);
   if (ok && !mbar_wait(bar_delta, 0)) {
     flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
     ok = false;
   }
   ok = __syncthreads_and(ok) != 0;
   if (ok) {
-    for (int c = h; c < p.BN / 32; c += 2) {
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      const int c = h + 2 * k;
+      if (c >= p.BN / 32) break;
       uint32_t v[32];
       tmem_ld_32x32b_x32(tmem_row + (uint32_t)(c * 32), v);
       tmem_ld_wait();
-      const int tc = t0 + c * 32;
-      const int tl = tc + lane;
-      int present = 0;
-      if (tl < p.T) {
-        const int a = p.tok_adapter[tl];
-        if (a >= 0) present = p.ptab[((int64_t)a * p.n_slots + p.slot) * kTabStride] >= 0;
-      }
-      const unsigned pmask = __ballot_sync(0xffffffffu, present);
+      const unsigned pmask = k == 0 ? pm[0] : k == 1 ? pm[1] : k == 2 ? pm[2] : pm[3];
       // y_s[col][feature] bf16 for the TMA store; delta_s[col][feature] fp32 from the TMA load
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const uint32_t col = (uint32_t)(c * 32 + i);
         float acc = __uint_as_float(v[i]);
-        if ((pmask >> i) & 1u) acc += ld_shared_f32(delta_s + (col * BM + row) * 4);
-        st_shared_u16(y_s + (col * BM + row) * 2, f32_to_bf16_rn(acc));
+        if ((pmask >> i) & 1u) acc += delta_p[col * BM + row];
+        y_p[col * BM + row] = f32_to_bf16_rn(acc);
       }
     }
     fence_proxy_async_shared();     // generic-proxy writes of y_s -> visible to the TMA store
@@ -403,7 +511,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   __syncthreads();
   if (threadIdx.x == 0 && ok) {
     tma_store_2d(&tm_y, m0, t0, y_s);             // rows past T and features past H are clipped
-    bulk_commit_and_wait_all();
+    bulk_commit_wait_read();                      // the kernel's completion publishes the writes
   }
   tc_fence_before();
   __syncthreads();
@@ -466,41 +574,59 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   }
   const int n_sm = device_sm_count();
   const int m_tiles = (G.H + BM - 1) / BM;
-  // Token tiles: as few as possible (<= 256 tokens each), but enough to fill about 3/4 of the
-  // SMs when the feature tiles alone do not (decode batches), down to 32-token tiles.
-  int n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
-  const int want = (3 * n_sm / 4 + m_tiles - 1) / m_tiles;
-  const int max_tiles = (G.T + 31) / 32;
-  if (n_tiles < want) n_tiles = want < max_tiles ? want : max_tiles;
-  int bn = (G.T + n_tiles - 1) / n_tiles;
-  bn = ((bn + 31) / 32) * 32;
-  if (bn > MAX_BN) bn = MAX_BN;
-  n_tiles = (G.T + bn - 1) / bn;
-  // Wide token tiles share each W tile across a cluster (multicast); for narrow tiles the
-  // per-SM shared-memory fill rate, not L2, is the limit, and the cluster only adds coupling.
-  const int cn = bn < 128 ? 1 : (n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1));
+  const int n_kb = G.H / BK;
+  int n_tiles, bn, cn, ks = 1;
+  const int ks_try = n_kb % 4 == 0 ? 4 : 2;
+  const int bn_try = ((G.T + 32 * ks_try - 1) / (32 * ks_try)) * (32 * ks_try);
+  if (G.T <= MAX_BN && n_kb % 2 == 0 && G.partials &&
+      (int64_t)(ks_try - 1) * bn_try * m_tiles * BM <= G.partials_floats) {
+    // One token tile holds the whole batch (decode): K is split over a cluster of 4 (or 2) CTAs
+    // per feature tile instead of cutting the tokens into narrow tiles, so each CTA streams
+    // a quarter of W's K range plus the matching quarter of x, and the partial sums meet in
+    // the scratch (L2).
+    ks = ks_try;
+    bn = bn_try;
+    n_tiles = 1;
+    cn = 1;
+  } else {
+    // Token tiles: as few as possible (<= 256 tokens each), but enough to fill about 3/4 of the
+    // SMs when the feature tiles alone do not, down to 32-token tiles.
+    n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
+    const int want = (3 * n_sm / 4 + m_tiles - 1) / m_tiles;
+    const int max_tiles = (G.T + 31) / 32;
+    if (n_tiles < want) n_tiles = want < max_tiles ? want : max_tiles;
+    bn = (G.T + n_tiles - 1) / n_tiles;
+    bn = ((bn + 31) / 32) * 32;
+    if (bn > MAX_BN) bn = MAX_BN;
+    n_tiles = (G.T + bn - 1) / bn;
+    // Wide token tiles share each W tile across a cluster (multicast); for narrow tiles the
+    // per-SM shared-memory fill rate, not L2, is the limit, and the cluster only adds coupling.
+    cn = bn < 128 ? 1 : (n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1));
+  }
   // Each pipeline stage costs a fixed handshake on top of its data, and a CTA's TMA fill rate is
   // bounded, so stages are made large: up to 4 K chunks of 64, at most 96 KB (>= 2 stages).
-  const int n_kb = G.H / BK;
+  const int kb_cta = n_kb / ks;
   const int chunk_bytes = A_BYTES + bn * BK * 2;
   int kc = 1;                       // wide tiles are MMA-bound: one chunk per stage
-  while (bn < 128 && kc < 4 && 2 * kc * chunk_bytes <= 96 * 1024 && n_kb % (2 * kc) == 0) kc *= 2;
+  while (bn < 128 && kc < 4 && 2 * kc * chunk_bytes <= 96 * 1024 && kb_cta % (2 * kc) == 0) kc *= 2;
   const int stage_bytes = kc * chunk_bytes;
   int stages = STAGE_AREA / stage_bytes;
   if (stages > MAX_STAGES) stages = MAX_STAGES;
+  const int ep_rows = bn / ks;      // token rows of the delta and y tiles one CTA's epilogue moves
   CUtensorMap tm_w, tm_x, tm_d, tm_y;
   int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)(BM / cn));
   if (rc != LORA_OK) return rc;
   rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
   if (rc != LORA_OK) return rc;
   // The delta tile the epilogue adds and the output tile it writes: [bn tokens][128 features].
-  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
+  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
   if (rc != LORA_OK) return rc;
-  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
+  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
   if (rc != LORA_OK) return rc;
   GemmParams P;
   P.y = G.y;
   P.delta = G.delta;
+  P.partials = G.partials;
   P.tok_adapter = G.tok_adapter;
   P.ptab = G.ptab;
   P.err = G.err;
@@ -511,16 +637,17 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.kc = kc;
   P.stages = stages;
   P.cn = cn;
+  P.ks = ks;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, m_tiles, n_tiles);
+  cfg.gridDim = dim3(ks, m_tiles, n_tiles);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.x = ks;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = cn;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -97,11 +97,19 @@ struct GemmLaunch {
   const float* delta;      // [T][H]
   const int32_t* tok_adapter;  // [T] validated ids
   const int32_t* ptab;
+  float* partials;         // split-K scratch (batches of <= 256 tokens)
+  int64_t partials_floats; // its capacity; the split is used only when it fits
   int32_t T, H, slot, n_slots;
   int32_t* err;
   bool pdl;
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
+// Capacity of the base GEMM's split-K scratch for a workspace of T_max tokens: 3 partial tiles
+// (4-way split) of up to 256 token columns, the tile rounded up to 128 columns.
+inline int64_t gemm_partial_floats(int32_t T_max, int32_t H) {
+  const int64_t t = T_max < 256 ? T_max : 256;
+  return 3 * ((t + 127) / 128 * 128) * (int64_t)H;
+}
 
 // Programmatic dependent launch: every kernel of the path waits for the kernel before it
 // (griddepcontrol.wait) before touching anything an earlier kernel writes, and only then

@@ -411,7 +411,7 @@ int lora_status(lora_pool* p, lora_stream_t stream) {
 // ---- segment workspace -----------------------------------------------------------------
 namespace {
 struct SegLayout {
-  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, total;
+  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials, total;
   int32_t max_seg, unit_cap;
 };
 SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
@@ -428,6 +428,7 @@ SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
   L.units = take((size_t)L.unit_cap * 16);
   L.n_units = take(16);
   L.delta = take((size_t)T_max * p->H * 4);
+  L.partials = take((size_t)gemm_partial_floats(T_max, p->H) * 4);
   L.total = off;
   return L;
 }
@@ -462,6 +463,7 @@ int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T
   seg->unit_cap = L.unit_cap;
   seg->reserved = 0;
   seg->delta = reinterpret_cast<float*>(b + L.delta);
+  seg->gemm_partials = reinterpret_cast<float*>(b + L.partials);
   return LORA_OK;
 }
 

@@ -99,6 +99,8 @@ typedef struct lora_segments {
   int32_t unit_cap;
   int32_t reserved;
   float*   delta;         /* [T_max][H]  (x_t A) B (fp32) */
+  float*   gemm_partials; /* [3][P][H] fp32 partial sums of the base GEMM for batches of <= 256
+                             tokens (K split over 4 CTAs); P = min(T_max, 256) rounded up to 128 */
 } lora_segments;
 
 /*
@@ -235,7 +237,7 @@ int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, 
  */
 #define LORA_NOALLOC_MAX_TOKENS 128
 #define LORA_NOALLOC_MAX_H 8192
-#define LORA_NOALLOC_SCRATCH_BYTES (4608 * 1024)
+#define LORA_NOALLOC_SCRATCH_BYTES (17 * 1024 * 1024)
 int lora_linear_forward_noalloc(lora_pool* pool, const int32_t* token_adapter, int32_t T, int32_t slot,
                                 const void* x, const void* W, void* y, lora_stream_t stream);
 
