@@ -129,7 +129,7 @@ def bf16_f64(bits):
 
 
 def check_close(y_gpu_bits, d_gpu, y_ref, d_ref, tag=""):
-    """north_star tolerance: |gpu - oracle| <= 1e-2 (1 + |oracle|) per element on y;
+    """The stated tolerance: |gpu - oracle| <= 1e-2 (1 + |oracle|) per element on y;
     relative L2 <= 5e-3 on the LoRA delta (read as fp32 from delta_dbg)."""
     y = bf16_f64(y_gpu_bits)
     bad = np.abs(y - y_ref) > 1e-2 * (1 + np.abs(y_ref))
