@@ -72,6 +72,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -519,6 +522,198 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
 }
 
+// ---- persistent variant (batches of more than 256 tokens) ---------------------------------
+// Each cluster of cn CTAs (cn token tiles sharing one W tile, W multicast as above) walks the
+// cluster tiles c, c + n_clusters, ...  TMEM holds two accumulators of BN columns.  Warp 0 issues
+// TMA loads without pause across tile boundaries, warp 1 issues the MMAs of tile i into
+// accumulator i % 2, and warps 4-7 (one per TMEM lane quarter) drain accumulator (i-1) % 2
+// meanwhile: add the delta (read straight from global memory), round to bf16, store y from
+// registers.  So a tile's epilogue runs under the next tile's main loop.
+struct PersistParams {
+  int32_t m_tiles, t_groups;       // feature tiles; token-tile groups of cn tiles
+  int32_t n_ctiles;                // m_tiles * t_groups
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, GemmParams p,
+                     PersistParams pp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGE_AREA);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 4);
+  const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * MAX_STAGES;
+  const uint32_t bar_tfull = bar_full + 16 * MAX_STAGES, bar_tempty = bar_tfull + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cn = p.cn;
+  const uint32_t crank = cn > 1 ? cluster_ctarank() : 0;
+  const uint16_t cmask = (uint16_t)((1u << cn) - 1u);
+  const int stages = p.stages;
+  const int kc = p.kc;
+  const uint32_t xb = (uint32_t)(p.BN * BK * 2);
+  const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
+  const int nk = p.n_kb / kc;
+  const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
+  const int n_clusters = (int)gridDim.x / cn;
+  const int cluster_id = (int)blockIdx.x / cn;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, (uint32_t)cn);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4);                 // one arrival per epilogue warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 2 * acc_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cn > 1) cluster_sync_all();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {                                    // TMA producer, all tiles back to back
+      const uint64_t pol_w = policy_evict_last();       // W tiles are re-read by other token tiles
+      const uint64_t pol_x = policy_evict_last();       // x tiles are re-read by other feature tiles
+      const int w_rows = BM / cn;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int ct = cluster_id; ct < pp.n_ctiles && ok; ct += n_clusters) {
+        const int m0 = (ct % pp.m_tiles) * BM;
+        const int t0 = ((ct / pp.m_tiles) * cn + (int)crank) * p.BN;
+        for (int i = 0; i < nk; ++i, ++it) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1;
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+            flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * s, stage_bytes);
+          const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+          for (int c = 0; c < kc; ++c) {
+            const int kx = (i * kc + c) * BK;
+            const uint32_t wdst = st + (uint32_t)c * A_BYTES;
+            if (cn > 1)
+              tma_load_2d_multicast(wdst + crank * (uint32_t)(w_rows * BK * 2), &tm_w, kx, m0 + (int)crank * w_rows,
+                                    bar_full + 8 * s, cmask, pol_w);
+            else
+              tma_load_2d(wdst, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
+            tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {                                    // MMA issuer
+      const uint32_t idesc = make_idesc_bf16(BM, p.BN);
+      uint32_t it = 0;
+      int tile = 0;
+      bool ok = true;
+      for (int ct = cluster_id; ct < pp.n_ctiles && ok; ct += n_clusters, ++tile) {
+        const int b = tile & 1;
+        if (!mbar_wait(bar_tempty + 8 * b, ((tile >> 1) & 1) ^ 1)) {   // accumulator b drained
+          flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)b * acc_cols;
+        for (int i = 0; i < nk; ++i, ++it) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1;
+          if (!mbar_wait(bar_full + 8 * s, ph)) {
+            flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+          for (int c = 0; c < kc; ++c) {
+            const uint64_t ad = sw128_kmajor_desc(st + (uint32_t)c * A_BYTES);
+            const uint64_t bd = sw128_kmajor_desc(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16_ss(acc, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
+          }
+          if (cn > 1)
+            mma_commit_multicast(bar_empty + 8 * s, cmask);
+          else
+            mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) mma_commit(bar_tfull + 8 * b);            // accumulator b complete
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- epilogue warps: TMEM lane quarter q = warp - 4 ----
+    const int q = warp - 4;
+    const int row = q * 32 + lane;
+    pdl_wait_then_release();                            // delta and ids come from earlier kernels
+    int tile = 0;
+    for (int ct = cluster_id; ct < pp.n_ctiles; ct += n_clusters, ++tile) {
+      const int b = tile & 1;
+      const int m0 = (ct % pp.m_tiles) * BM;
+      const int t0 = ((ct / pp.m_tiles) * cn + (int)crank) * p.BN;
+      const int feat = m0 + row;
+      bool ok = mbar_wait(bar_tfull + 8 * b, (tile >> 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc_row = tmem + (uint32_t)b * acc_cols + ((uint32_t)(q * 32) << 16);
+      const int n_chunks = p.BN / 32;
+      for (int c4 = 0; c4 < n_chunks; c4 += 4) {
+        unsigned pm[4];
+        presence_masks(p, t0, c4, 1, n_chunks, lane, pm);
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          const int c = c4 + k;
+          if (c >= n_chunks) break;
+          const int tc = t0 + c * 32;
+          if (tc >= p.T) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(acc_row + (uint32_t)(c * 32), v);
+          tmem_ld_wait();
+          const unsigned pmask = k == 0 ? pm[0] : k == 1 ? pm[1] : k == 2 ? pm[2] : pm[3];
+          if (feat < p.H) {
+            // every load of the chunk before its first store (y may alias delta as far as the
+            // compiler knows)
+            float dv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              dv[i] = ((pmask >> i) & 1u) ? __ldg(p.delta + (size_t)(tc + i) * p.H + feat) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float a = __uint_as_float(v[i]);
+              if (tc + i < p.T) p.y[(size_t)(tc + i) * p.H + feat] = f32_to_bf16_rn((pmask >> i) & 1u ? a + dv[i] : a);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);   // accumulator b may be overwritten
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 2 * acc_cols);
+  if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
+}
+
 // ---- host side --------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -565,12 +760,46 @@ int encode_2d_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 
 }  // namespace
 
+namespace {
+// Clusters of `cn` persistent CTAs that can be resident at once (cached per device and cn).
+int persistent_clusters(int cn) {
+  static int cached[64][5] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev][cn] > 0) return cached[dev][cn];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cn * 64);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cn;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_lora_persistent, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = device_sm_count() / cn;
+  }
+  cached[dev][cn] = n;
+  return n;
+}
+}  // namespace
+
 int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(gemm_lora_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return lora_cuda_fail(e, "gemm_lora_kernel attribute");
-    attr_set = true;
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_lora_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return lora_cuda_fail(e, "gemm kernel attribute");
+    attr_set[dev] = true;
   }
   const int n_sm = device_sm_count();
   const int m_tiles = (G.H + BM - 1) / BM;
@@ -613,6 +842,11 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   int stages = STAGE_AREA / stage_bytes;
   if (stages > MAX_STAGES) stages = MAX_STAGES;
   const int ep_rows = bn / ks;      // token rows of the delta and y tiles one CTA's epilogue moves
+  // More tiles than resident CTAs: persistent CTAs overlap each tile's epilogue with the next
+  // tile's main loop.
+  const int n_ctiles = m_tiles * (n_tiles / cn);
+  const int n_clusters_res = ks == 1 ? persistent_clusters(cn) : 0;
+  const bool persistent = ks == 1 && n_ctiles > n_clusters_res;
   CUtensorMap tm_w, tm_x, tm_d, tm_y;
   int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)(BM / cn));
   if (rc != LORA_OK) return rc;
@@ -640,6 +874,29 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.ks = ks;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
+  if (persistent) {
+    PersistParams pp;
+    pp.m_tiles = m_tiles;
+    pp.t_groups = n_tiles / cn;
+    pp.n_ctiles = n_ctiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_clusters_res * cn);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = cn;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = G.pdl ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_persistent, tm_w, tm_x, P, pp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks, m_tiles, n_tiles);
   cfg.blockDim = dim3(THREADS);

@@ -86,8 +86,10 @@ SMALL = [
     (384, 300, [16, 40], 1, 0.5),
     (512, 520, [64, 8, 33, 17, 2, 9, 12, 63], 2, 0.15),
     (1024, 96, [32, 64, 8, 16], 4, 0.2),
-    (2048, 256, [64, 8, 16, 32, 1], 1, 0.2),     # base GEMM splits K over a cluster of 8
+    (2048, 256, [64, 8, 16, 32, 1], 1, 0.2),     # base GEMM splits K over a cluster of 4
     (1216, 64, [16, 64, 3], 2, 0.3),            # uneven 2-way K split, ragged last feature tile
+    (2048, 2600, [16, 64, 8, 32], 1, 0.2),      # persistent GEMM, 176 tiles, ragged last token tile
+    (1024, 9700, [8, 16, 64], 1, 0.1),          # persistent GEMM with W multicast over 2 token tiles
 ]
 
 
