@@ -39,22 +39,25 @@ namespace {
 constexpr int kCluster = 4;                    // CTAs per unit, one feature quarter each
 constexpr int kUnitTok = kUnitTokens;         // tokens per unit (16)
 constexpr int kFB = 1024;                      // features per stage row (one feature block)
-constexpr int kRows = 16;                      // rows per stage
-constexpr int kStages = 5;
+constexpr int kRows = 32;                      // page rows per ring stage: two groups of 16
+constexpr int kStages = 2;                     // ring stages
+constexpr int kXRows = kUnitTok;               // x rows of the unit: a buffer of their own
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;      // + one producer warp
-// Stage rows are padded by 16 bytes so that the 8 rows an ldmatrix phase reads fall in 8
+// Staged rows are padded by 16 bytes so that the 8 rows an ldmatrix phase reads fall in 8
 // different 16-byte bank groups.
-constexpr int kSlotBytes = kRows * (kFB * 2 + 16);
+constexpr int kRowBytes = kFB * 2 + 16;
+constexpr int kSlotBytes = kRows * kRowBytes;
 constexpr int kSbPitch = LORA_MAX_RANK + 8;    // bf16 elements per token row of s (hi or lo)
 // shared memory layout (dynamic)
 constexpr int kOffRing = 0;
-constexpr int kOffPart = kOffRing + kStages * kSlotBytes;                    // [8 warps][16][16] f32
+constexpr int kOffX = kOffRing + kStages * kSlotBytes;                       // [16 tokens][kRowBytes]
+constexpr int kOffPart = kOffX + kXRows * kRowBytes;                         // [8 warps][16][16] f32
 constexpr int kOffExch = kOffPart + kConsumerWarps * 16 * 16 * 4;            // [2][4][64][16] f32
 constexpr int kOffSb = kOffExch + 2 * kCluster * LORA_MAX_RANK * kUnitTok * 4;  // [2][16][kSbPitch] bf16
 constexpr int kOffBar = kOffSb + 2 * kUnitTok * kSbPitch * 2;
-constexpr int kSmemBytes = kOffBar + (2 * kStages + 2) * 8;
+constexpr int kSmemBytes = kOffBar + (2 * kStages + 4) * 8;
 static_assert(kUnitTok == 16, "the MMA tiling assumes 16 tokens per unit");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffSb % 16 == 0 && kOffBar % 8 == 0, "alignment");
@@ -212,6 +215,8 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   const uint32_t bar_full = smem_u32(smem + kOffBar);
   const uint32_t bar_empty = bar_full + 8 * kStages;
   const uint32_t bar_exch = bar_empty + 8 * kStages;
+  const uint32_t bar_xfull = bar_exch + 16, bar_xempty = bar_xfull + 8;
+  const uint32_t xbuf = smem_u32(smem + kOffX);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -219,6 +224,8 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int b = 0; b < 2; ++b) mbar_init(bar_exch + 8 * b, 1);
+    mbar_init(bar_xfull, 1);
+    mbar_init(bar_xempty, kConsumerWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   cluster_sync_all();                                     // peers' barriers exist before any remote access
@@ -237,7 +244,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     // Unit records and page ids are loaded one unit ahead, so their latency hides behind the
     // copies of the current unit.
     auto tok_lane = [](int l, int) { return l; };
-    uint32_t it = 0;
+    uint32_t it = 0, xi = 0;                              // ring stages and x buffer fills issued
     bool ok = true;
     int4 rec = load_rec(seg, group, n_units);
     Gathered G;
@@ -257,29 +264,34 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             G.pa[h] = G.pb[h] = -1;                       // the column is dropped on both sides
           }
         }
-        const int ng = (U.r + 15) / 16;
-        // stages in consumption order: per feature block, x then the A groups; then the B groups
+        const int nq = (U.r + 31) / 32;                   // stages of up to 32 rank columns
+        // in consumption order: per feature block, the x rows (own buffer) then the A stages;
+        // then the B stages.  Lane l copies rank column 32q + l of stage q.
         for (int phase = 0; phase < 2 && ok; ++phase) {
           for (int fb = 0; fb < n_fb && ok; ++fb) {
             const int fw = min(kFB, Hq - fb * kFB);
             const int f0 = f_cta + fb * kFB;
-            const uint32_t pitch = fw * 2 + 16;
-            for (int g = (phase == 0 ? -1 : 0); g < ng; ++g) {
+            if (phase == 0) {                              // x rows of the unit's tokens
+              ok = __all_sync(0xffffffffu, mbar_wait(bar_xempty, (xi & 1) ^ 1));
+              if (!ok) break;
+              const bool mine = lane < U.n_tok;
+              const uint32_t rows = __popc(__ballot_sync(0xffffffffu, mine));
+              if (lane == 0) mbar_arrive_expect_tx(bar_xfull, rows * fw * 2);
+              __syncwarp();
+              if (mine) bulk_g2s(xbuf + lane * kRowBytes, L.x + (int64_t)G.tok[0] * H + f0, fw * 2, bar_xfull);
+              ++xi;
+            }
+            for (int q = 0; q < nq; ++q) {
               const int s = it % kStages;
               ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1));
               if (!ok) break;
-              const uint16_t* src = nullptr;
-              if (g < 0) {                                 // x rows of the unit's tokens
-                if (lane < U.n_tok) src = L.x + (int64_t)G.tok[0] * H + f0;
-              } else {
-                const int32_t* pg = phase == 0 ? G.pa : G.pb;
-                const int32_t page = __shfl_sync(0xffffffffu, (g >> 1) ? pg[1] : pg[0], 16 * (g & 1) + (lane & 15));
-                if (lane < 16 && page >= 0) src = L.pool + (int64_t)page * H + f0;
-              }
-              const uint32_t rows = __popc(__ballot_sync(0xffffffffu, src != nullptr));
+              const int32_t page = q ? (phase == 0 ? G.pa[1] : G.pb[1]) : (phase == 0 ? G.pa[0] : G.pb[0]);
+              const bool mine = page >= 0;
+              const uint32_t rows = __popc(__ballot_sync(0xffffffffu, mine));
               if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, rows * fw * 2);
               __syncwarp();
-              if (src) bulk_g2s(ring + s * kSlotBytes + lane * pitch, src, fw * 2, bar_full + 8 * s);
+              if (mine) bulk_g2s(ring + s * kSlotBytes + lane * kRowBytes, L.pool + (int64_t)page * H + f0, fw * 2,
+                                 bar_full + 8 * s);
               ++it;
             }
           }
@@ -289,17 +301,19 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
       G = Gn;
     }
     if (!ok) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
-    // Drain: the most recent use of every slot has landed before the CTA can exit.
-    if (lane == 0)
+    // Drain: the most recent use of every slot and of the x buffer has landed before exit.
+    if (lane == 0) {
       for (uint32_t k = it > (uint32_t)kStages ? it - kStages : 0; k < it; ++k)
         if (!mbar_wait(bar_full + 8 * (k % kStages), (k / kStages) & 1)) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
+      if (xi > 0 && !mbar_wait(bar_xfull, (xi - 1) & 1)) flag_error(L.err, LORA_DEV_WAIT_TIMEOUT);
+    }
   } else {
     // ================================ consumer warps ================================
     // After a failed wait the warps keep walking the same sequence of units, stages and barriers
     // (skipping the waits), so every named and cluster barrier still sees all its threads.
     // Lane l stores delta for tokens tok_store(l, k), k < 4 (the MMA accumulator layout).
     auto tok_store = [](int l, int k) { return (k >> 1) * 8 + 2 * (l & 3) + (k & 1); };
-    uint32_t it = 0, n_done = 0;
+    uint32_t it = 0, n_done = 0, xi = 0;
     bool ok = true;
     const int mi = lane >> 3, ri = lane & 7;              // ldmatrix: matrix and row this lane addresses
     __nv_bfloat16* sb_hi = sb;
@@ -322,21 +336,19 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
 
         // ---- shrink over this CTA's feature quarter: acc[n-tile] = A_g^T x^T (16 pages x 8 tokens)
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int nq = (U.r + 31) / 32;
         for (int fb = 0; fb < n_fb; ++fb) {
           const int fw = min(kFB, Hq - fb * kFB);
-          const uint32_t pitch = fw * 2 + 16;
-          const int sx = it % kStages;
-          ok = ok && wait_warp(bar_full + 8 * sx, (it / kStages) & 1);
-          ++it;
-          const uint32_t xbase = ring + sx * kSlotBytes;
-          for (int g = 0; g < ng; ++g) {
+          ok = ok && wait_warp(bar_xfull, xi & 1);
+          ++xi;
+          for (int q = 0; q < nq; ++q) {
             const int s = it % kStages;
             ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
             ++it;
-            if (ok && g == my_g) {
-              const uint32_t abase = ring + s * kSlotBytes;
-              const uint32_t a_row = abase + (ri + 8 * (mi & 1)) * pitch + 16 * (mi >> 1);
-              const uint32_t x_row = xbase + (ri + 8 * (mi >> 1)) * pitch + 16 * (mi & 1);
+            if (ok && (my_g >> 1) == q && my_g < ng) {   // this warp's group: rows 16*(my_g&1) ..
+              const uint32_t abase = ring + s * kSlotBytes + (my_g & 1) * 16 * kRowBytes;
+              const uint32_t a_row = abase + (ri + 8 * (mi & 1)) * kRowBytes + 16 * (mi >> 1);
+              const uint32_t x_row = xbuf + (ri + 8 * (mi >> 1)) * kRowBytes + 16 * (mi & 1);
 #pragma unroll 4
               for (int ks = sub; ks < fw / 16; ks += wpg) {
                 uint32_t af[4], xf[4];
@@ -350,7 +362,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_empty + 8 * sx);
+          if (lane == 0) mbar_arrive(bar_xempty);            // the x rows may be replaced
         }
         // partial sums of this warp: part[warp][page][token]
         if (my_g < ng) {
@@ -399,7 +411,6 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
         // ---- expand: delta[t][f] for this CTA's features, warp w owns 128 features per block
         for (int fb = 0; fb < n_fb; ++fb) {
           const int fw = min(kFB, Hq - fb * kFB);
-          const uint32_t pitch = fw * 2 + 16;
           const int f_warp = warp * 128;
           float e[8][2][4];
 #pragma unroll
@@ -408,11 +419,11 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int k = 0; k < 4; ++k) e[mt][nt][k] = 0.f;
-          for (int g = 0; g < ng; ++g) {
+          for (int q = 0; q < nq; ++q) {
             const int s = it % kStages;
             ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
             ++it;
-            if (ok && f_warp < fw) {
+            for (int g = 2 * q; g < min(ng, 2 * q + 2) && ok && f_warp < fw; ++g) {
               uint32_t sh[4], sl[4];
               const uint32_t s_off = ((ri + 8 * (mi >> 1)) * kSbPitch + 16 * g + 8 * (mi & 1)) * 2;
               ldsm_x4(smem_u32(sb_hi) + s_off, sh);
@@ -421,7 +432,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
               const uint32_t kb = 16 * g + 2 * (lane & 3);
               const uint32_t m01 = (((vm >> kb) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 1)) & 1) ? 0xFFFF0000u : 0u);
               const uint32_t m23 = (((vm >> (kb + 8)) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 9)) & 1) ? 0xFFFF0000u : 0u);
-              const uint32_t b_row = ring + s * kSlotBytes + (ri + 8 * (mi >> 1)) * pitch + 16 * (mi & 1);
+              const uint32_t b_row = ring + s * kSlotBytes + ((g & 1) * 16 + ri + 8 * (mi >> 1)) * kRowBytes + 16 * (mi & 1);
 #pragma unroll
               for (int mt = 0; mt < 8; ++mt) {
                 if (f_warp + mt * 16 < fw) {
