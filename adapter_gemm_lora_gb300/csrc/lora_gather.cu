@@ -238,6 +238,10 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   const int n_units = *seg.n_units;
   const int n_groups = gridDim.x / kCluster;
   const int group = blockIdx.x / kCluster;
+  // Units are dealt to the clusters in waves of n_groups, alternately left to right and right
+  // to left.  The list comes largest ranks first, so a cluster that draws one of the longest
+  // units of a wave draws one of the shortest of the next.  unit_at grows with w.
+  auto unit_at = [n_groups, group](int w) { return w * n_groups + ((w & 1) ? n_groups - 1 - group : group); };
 
   if (warp == kConsumerWarps) {
     // ================================ producer warp ================================
@@ -246,16 +250,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     auto tok_lane = [](int l, int) { return l; };
     uint32_t it = 0, xi = 0;                              // ring stages and x buffer fills issued
     bool ok = true;
-    int4 rec = load_rec(seg, group, n_units);
+    int4 rec = load_rec(seg, unit_at(0), n_units);
     Gathered G;
     Unit U = unit_of(L, rec);
     gather_issue<1>(seg, U, lane, tok_lane, G);
-    int4 rec_next = load_rec(seg, group + n_groups, n_units);
-    for (int u = group; u < n_units && ok; u += n_groups) {   // the producer alone may stop early
+    int4 rec_next = load_rec(seg, unit_at(1), n_units);
+    for (int w = 0; unit_at(w) < n_units && ok; ++w) {   // the producer alone may stop early
       const Unit Un = unit_of(L, rec_next);
       Gathered Gn;
       gather_issue<1>(seg, Un, lane, tok_lane, Gn);
-      rec_next = load_rec(seg, u + 2 * n_groups, n_units);
+      rec_next = load_rec(seg, unit_at(w + 2), n_units);
       if (slot_has_lora(G)) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -318,16 +322,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     const int mi = lane >> 3, ri = lane & 7;              // ldmatrix: matrix and row this lane addresses
     __nv_bfloat16* sb_hi = sb;
     __nv_bfloat16* sb_lo = sb + kUnitTok * kSbPitch;
-    int4 rec = load_rec(seg, group, n_units);
+    int4 rec = load_rec(seg, unit_at(0), n_units);
     Gathered G;
     Unit U = unit_of(L, rec);
     gather_issue<4>(seg, U, lane, tok_store, G);
-    int4 rec_next = load_rec(seg, group + n_groups, n_units);
-    for (int u = group; u < n_units; u += n_groups) {
+    int4 rec_next = load_rec(seg, unit_at(1), n_units);
+    for (int w = 0; unit_at(w) < n_units; ++w) {
       const Unit Un = unit_of(L, rec_next);
       Gathered Gn;
       gather_issue<4>(seg, Un, lane, tok_store, Gn);
-      rec_next = load_rec(seg, u + 2 * n_groups, n_units);
+      rec_next = load_rec(seg, unit_at(w + 2), n_units);
       if (slot_has_lora(G)) {
         const uint64_t vm = valid_mask(G, U.r, L.num_pages, lane);
         const int ng = (U.r + 15) / 16;

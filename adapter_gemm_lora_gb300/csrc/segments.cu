@@ -7,10 +7,10 @@
 // adapter (-1) first and outside every segment.
 //
 // One CTA of 1024 threads: a shared-memory histogram over adapter ids (with each used
-// adapter's rank), one block scan that turns counts into run starts, segment indices and the
-// offsets of the LoRA-delta work units (each written right away as a complete record:
-// adapter, rank, first index into perm, token count), then a stable scatter in chunks of
-// 1024 tokens (warp-level match for ranks inside a warp, warps in order).
+// adapter's rank), two block scans that turn counts into run starts, segment indices and the
+// offsets of the LoRA-delta work units within their rank class (each unit written right away
+// as a complete record: adapter, rank, first index into perm, token count), then a stable
+// scatter in chunks of 1024 tokens (warp-level match for ranks inside a warp, warps in order).
 #include <cuda_runtime.h>
 
 #include "lora_internal.h"
@@ -24,6 +24,9 @@ __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
   atomicCAS(err, 0, LORA_EDEVICE);
   atomicOr(err + 1, bits);
 }
+
+// Work-unit cost class of a rank: 0 for 33..64, 1 for 17..32, 2 for 9..16, 3 for 1..8.
+__device__ __forceinline__ int rank_class(int32_t r) { return r > 32 ? 0 : r > 16 ? 1 : r > 8 ? 2 : 3; }
 
 // Exclusive block scan of four int32 values per thread; totals land in tot[0..3].
 __device__ __forceinline__ void block_exclusive_scan4(int32_t (&v)[4], int32_t (*sh)[33], int32_t (&tot)[4]) {
@@ -97,30 +100,40 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   }
   __syncthreads();
 
-  // 2. one scan gives run starts, segment indices and both work-list offsets; each thread then
-  //    writes the segments and work units of its own keys
+  // 2. one scan gives run starts and segment indices, a second one the work-unit offsets
+  //    inside each rank class; each thread then writes the segments and work units of its own
+  //    keys.  Units are listed by rank class, largest ranks first (a unit's cost grows with
+  //    the pages it gathers), then by adapter id and token offset, so that the delta kernel,
+  //    which deals units to its clusters in waves, starts the longest ones first.
   const int per = (K + kThreads - 1) / kThreads;
   const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
-  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, work units, -
+  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, -, -
+  int32_t ub[4] = {0, 0, 0, 0};                // work units per rank class
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     v[0] += c;
     if (k > 0 && c > 0) {
       v[1] += 1;
-      v[2] += (c + kUnitTokens - 1) / kUnitTokens;
+      ub[rank_class(krank[k])] += (c + kUnitTokens - 1) / kUnitTokens;
     }
   }
-  int32_t tot[4];
+  int32_t tot[4], utot[4];
   block_exclusive_scan4(v, sh_scan, tot);
+  block_exclusive_scan4(ub, sh_scan, utot);
+  ub[1] += utot[0];
+  ub[2] += utot[0] + utot[1];
+  ub[3] += utot[0] + utot[1] + utot[2];
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     if (k > 0 && c > 0) {
       const int32_t sidx = v[1];
       seg.seg_off[sidx] = v[0];
       seg.seg_adapter[sidx] = k - 1;
-      for (int b = 0; b * kUnitTokens < c; ++b, ++v[2])
-        reinterpret_cast<int4*>(seg.units)[v[2]] =
-            make_int4(k - 1, krank[k], v[0] + b * kUnitTokens, min(kUnitTokens, c - b * kUnitTokens));
+      const int32_t r = krank[k];
+      int32_t& u = ub[rank_class(r)];
+      for (int b = 0; b * kUnitTokens < c; ++b, ++u)
+        reinterpret_cast<int4*>(seg.units)[u] =
+            make_int4(k - 1, r, v[0] + b * kUnitTokens, min(kUnitTokens, c - b * kUnitTokens));
       ++v[1];
     }
     cnt[k] = v[0];                             // becomes the running write position of key k
@@ -131,7 +144,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
     seg.seg_off[S] = T;
     if (S == 0) seg.seg_off[0] = T;
     *seg.n_seg = S;
-    *seg.n_units = tot[2];
+    *seg.n_units = utot[0] + utot[1] + utot[2] + utot[3];
   }
   __syncthreads();
 

@@ -79,7 +79,8 @@ typedef struct lora_pool_stats_t {
  *   n_seg[1]         S;
  *   units[4 U]       LoRA-delta work units, U = *n_units: unit u covers the tokens
  *                    perm[units[4u+2] .. units[4u+2] + units[4u+3]) (at most 16, all of one
- *                    segment) of adapter units[4u], whose rank is units[4u+1];
+ *                    segment) of adapter units[4u], whose rank is units[4u+1]; listed by
+ *                    rank class (33..64, 17..32, 9..16, 1..8), then adapter id, then offset;
  * plus the fp32 scratch for the LoRA delta used by lora_linear_forward.  Calls that use
  * the same workspace must be ordered on one stream: the scratch is reused by every
  * projection slot.

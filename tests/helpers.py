@@ -109,6 +109,13 @@ class DeviceScene:
         return (self.read_i32(self.seg.perm, T), self.read_i32(self.seg.seg_off, n_seg + 1),
                 self.read_i32(self.seg.seg_adapter, n_seg))
 
+    def read_units(self):
+        """The LoRA-delta work list of the last build: int32 [U][4] (adapter, rank, first, count)."""
+        import torch
+        torch.cuda.synchronize()
+        n_units = int(self.read_i32(self.seg.n_units, 1)[0])
+        return self.read_i32(self.seg.units, 4 * n_units).reshape(n_units, 4)
+
     def forward(self, slot, x_t, W_t, with_delta=True, stream=None):
         import torch
         T = x_t.shape[0]

@@ -1,4 +1,6 @@
 """CUDA path vs the oracle, element by element, through the C boundary (GB300 only)."""
+import zlib
+
 import numpy as np
 import pytest
 
@@ -34,7 +36,7 @@ def _run_slot(sc, ta, slot, x_bits, W_bits, tokens=None):
 # ---------------------------------------------------------------------------- segments
 @pytest.mark.parametrize("case", ["random", "all_none", "all_distinct", "single", "one_token", "empty", "long"])
 def test_segments_bit_exact(L, case):
-    rng = np.random.default_rng(hash(case) % 1000)
+    rng = np.random.default_rng(zlib.crc32(case.encode()))
     n_ad = 40
     ta = {"random": lambda: rng.integers(-1, n_ad, size=777),
           "all_none": lambda: np.full(100, -1),
@@ -43,7 +45,8 @@ def test_segments_bit_exact(L, case):
           "one_token": lambda: np.array([5]),
           "empty": lambda: np.zeros(0, dtype=np.int64),
           "long": lambda: rng.integers(-1, n_ad, size=5000)}[case]().astype(np.int32)
-    wl = workloads.small(H=64, T=max(len(ta), 1), n_adapters=n_ad, ranks=[1 + (a % 8) for a in range(n_ad)], seed=1)
+    ranks = [(3, 12, 24, 64, 8, 40, 17, 9)[a % 8] for a in range(n_ad)]     # every rank class
+    wl = workloads.small(H=64, T=max(len(ta), 1), n_adapters=n_ad, ranks=ranks, seed=1)
     sc = DeviceScene(L, wl)
     sc.segments(ta)
     perm, off, sa = sc.read_segments()
@@ -51,6 +54,16 @@ def test_segments_bit_exact(L, case):
     assert np.array_equal(perm, w_perm)
     assert np.array_equal(off, w_off)
     assert np.array_equal(sa, w_sa)
+    # the work list: every segment cut into runs of <= 16 tokens, listed by rank class
+    # (33..64, 17..32, 9..16, 1..8), then adapter id, then offset
+    want = []
+    for s in range(len(w_sa)):
+        a, lo, hi = int(w_sa[s]), int(w_off[s]), int(w_off[s + 1])
+        r = int(wl.ranks[a])
+        cls = 0 if r > 32 else 1 if r > 16 else 2 if r > 8 else 3
+        want += [(cls, a, b, r, min(16, hi - b)) for b in range(lo, hi, 16)]
+    want = np.array([(a, r, b, n) for _, a, b, r, n in sorted(want)], dtype=np.int32).reshape(-1, 4)
+    assert np.array_equal(sc.read_units(), want)
     L.lora_status(sc.pool)
     sc.close()
 
