@@ -32,13 +32,15 @@ LORA_EDEVICE = -7
 LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 16384
 LORA_MAX_TOKENS = 65536
+LORA_MAX_GROUP = 4
 LORA_NOALLOC_MAX_TOKENS = 128
 LORA_NOALLOC_MAX_H = 8192
 
 EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_adapter_load",
             "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",
             "lora_linear_forward", "lora_status", "lora_pool_stats", "lora_last_error", "lora_pool_destroy",
-            "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc"]
+            "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc",
+            "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group"]
 KINDS = ("segments", "delta", "gemm", "scatter")
 
 
@@ -53,7 +55,7 @@ class lora_segments(ctypes.Structure):
     _fields_ = [("T_max", ctypes.c_int32), ("T", ctypes.c_int32), ("max_seg", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("perm", ctypes.c_void_p), ("seg_off", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
                 ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("units", ctypes.c_void_p),
-                ("n_units", ctypes.c_void_p), ("unit_cap", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_units", ctypes.c_void_p), ("unit_cap", ctypes.c_int32), ("delta_slots", ctypes.c_int32),
                 ("delta", ctypes.c_void_p), ("gemm_partials", ctypes.c_void_p)]
 
 
@@ -92,6 +94,9 @@ def _load():
         "lora_profile_enable": (I32, [VP, I32]),
         "lora_profile_read": (I32, [VP, I32, VP, VP, I32]),
         "lora_linear_forward_noalloc": (I32, [VP, VP, I32, I32, VP, VP, VP, VP]),
+        "lora_segments_size_group": (I64, [VP, I32, I32]),
+        "lora_segments_init_group": (I32, [VP, VP, I64, I32, I32, P(lora_segments)]),
+        "lora_linear_forward_group": (I32, [VP, P(lora_segments), I32, VP, VP, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -202,6 +207,20 @@ def lora_segments_init(pool, workspace_dev, workspace_bytes: int, T_max: int) ->
     return seg
 
 
+def lora_segments_size_group(pool, T_max: int, max_group: int) -> int:
+    n = _load().lora_segments_size_group(pool, T_max, max_group)
+    if n < 0:
+        raise LoraError(int(n), lora_last_error())
+    return int(n)
+
+
+def lora_segments_init_group(pool, workspace_dev, workspace_bytes: int, T_max: int, max_group: int) -> lora_segments:
+    seg = lora_segments()
+    _check(_load().lora_segments_init_group(pool, _ptr(workspace_dev), workspace_bytes, T_max, max_group,
+                                            ctypes.byref(seg)))
+    return seg
+
+
 def lora_segments_build(pool, token_adapter_dev, T: int, seg: lora_segments, stream=None) -> None:
     _check(_load().lora_segments_build(pool, _ptr(token_adapter_dev), T, ctypes.byref(seg), _stream(stream)))
 
@@ -210,6 +229,20 @@ def lora_linear_forward(pool, seg: lora_segments, slot: int, x_dev, W_dev, y_dev
                         stream=None) -> None:
     _check(_load().lora_linear_forward(pool, ctypes.byref(seg), slot, _ptr(x_dev), _ptr(W_dev), _ptr(y_dev),
                                        _ptr(delta_dbg_dev), _stream(stream)))
+
+
+def lora_linear_forward_group(pool, seg: lora_segments, slots: Sequence[int], x_dev, W_devs, y_devs,
+                              delta_dbg_devs=None, stream=None) -> None:
+    """Several slots that read the same x (q, k, v of a layer): one LoRA-delta launch for all."""
+    n = len(slots)
+    sl = np.ascontiguousarray(slots, dtype=np.int32)
+    Ws = (ctypes.c_void_p * n)(*[_ptr(w) for w in W_devs])
+    ys = (ctypes.c_void_p * n)(*[_ptr(v) for v in y_devs])
+    ds = None if delta_dbg_devs is None else (ctypes.c_void_p * n)(*[_ptr(d) for d in delta_dbg_devs])
+    _check(_load().lora_linear_forward_group(pool, ctypes.byref(seg), n, _ptr(sl), _ptr(x_dev),
+                                             ctypes.cast(Ws, ctypes.c_void_p), ctypes.cast(ys, ctypes.c_void_p),
+                                             ctypes.cast(ds, ctypes.c_void_p) if ds is not None else None,
+                                             _stream(stream)))
 
 
 def lora_status(pool, stream=None) -> None:

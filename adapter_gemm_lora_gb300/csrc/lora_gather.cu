@@ -8,7 +8,10 @@
 //   expand  delta[t, n] = sum_j s[t, j] * B[j, n]        (B page j = row j of B, H values)
 //
 // Work unit: up to 16 tokens of one segment (tokens that share an adapter), handled by a
-// cluster of 4 CTAs.  CTA q owns one quarter of the feature range, [q H/4, (q+1) H/4), for
+// cluster of 4 CTAs.  One launch may serve several projection slots that read the same x
+// (q, k and v of a layer): its work items are then every unit once per slot, each with its
+// slot's page table and delta buffer, so the short per-slot work lists of a decode batch
+// become one list long enough to keep every cluster busy.  CTA q owns one quarter of the feature range, [q H/4, (q+1) H/4), for
 // both products: it reads that quarter of the unit's token rows of x, of all r A pages and of
 // all r B pages, and nothing else.  The shrink over its quarter gives partial sums of s; the
 // four partials are exchanged through distributed shared memory and added in a fixed order,
@@ -142,21 +145,33 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One work unit as the segment builder wrote it, plus the per-lane entries a warp gathers for
-// it: the page ids of rank columns lane and lane + 32 (-1 past the rank) and perm entries.
+// One work item: a work unit as the segment builder wrote it, for one slot of the launch's
+// group, plus the per-lane entries a warp gathers for it: the page ids of rank columns lane
+// and lane + 32 (-1 past the rank) and perm entries.
 struct Unit {
   int r, t_begin, n_tok;
-  const int32_t* tab;
+  const int32_t* tab;      // the adapter's page table on the item's slot
+  float* delta;            // the slot's delta rows
 };
 __device__ __forceinline__ int4 load_rec(const lora_segments& seg, int u, int n_units) {
   return u < n_units ? __ldg(reinterpret_cast<const int4*>(seg.units) + u) : make_int4(0, 0, 0, 0);
 }
-__device__ __forceinline__ Unit unit_of(const LoraLaunch& L, const int4& rec) {
+// Item i of the launch is unit i / n_group on group member i % n_group.
+__device__ __forceinline__ Unit unit_of(const LoraLaunch& L, const int4& rec, int g) {
   Unit U;
   U.r = rec.y;
   U.t_begin = rec.z;
   U.n_tok = rec.w;
-  U.tab = L.ptab + ((int64_t)rec.x * L.n_slots + L.slot) * kTabStride;
+  int slot = L.slot[0];
+  float* d = L.delta[0];
+#pragma unroll
+  for (int k = 1; k < LORA_MAX_GROUP; ++k)
+    if (g == k) {
+      slot = L.slot[k];
+      d = L.delta[k];
+    }
+  U.tab = L.ptab + ((int64_t)rec.x * L.n_slots + slot) * kTabStride;
+  U.delta = d;
   return U;
 }
 struct Gathered {
@@ -236,12 +251,14 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   const int n_fb = (Hq + kFB - 1) / kFB;
   const int f_cta = (int)q * Hq;
   const int n_units = *seg.n_units;
+  const int ng = L.n_group;
+  const int n_items = n_units * ng;                       // item i: unit i / ng on member i % ng
   const int n_groups = gridDim.x / kCluster;
   const int group = blockIdx.x / kCluster;
-  // Units are dealt to the clusters in waves of n_groups, alternately left to right and right
-  // to left.  The list comes largest ranks first, so a cluster that draws one of the longest
-  // units of a wave draws one of the shortest of the next.  unit_at grows with w.
-  auto unit_at = [n_groups, group](int w) { return w * n_groups + ((w & 1) ? n_groups - 1 - group : group); };
+  // Items are dealt to the clusters in waves of n_groups, alternately left to right and right
+  // to left.  Units come largest ranks first, so a cluster that draws one of the longest items
+  // of a wave draws one of the shortest of the next.  item_at grows with w.
+  auto item_at = [n_groups, group](int w) { return w * n_groups + ((w & 1) ? n_groups - 1 - group : group); };
 
   if (warp == kConsumerWarps) {
     // ================================ producer warp ================================
@@ -250,16 +267,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     auto tok_lane = [](int l, int) { return l; };
     uint32_t it = 0, xi = 0;                              // ring stages and x buffer fills issued
     bool ok = true;
-    int4 rec = load_rec(seg, unit_at(0), n_units);
+    int4 rec = load_rec(seg, item_at(0) / ng, n_units);
     Gathered G;
-    Unit U = unit_of(L, rec);
+    Unit U = unit_of(L, rec, item_at(0) % ng);
     gather_issue<1>(seg, U, lane, tok_lane, G);
-    int4 rec_next = load_rec(seg, unit_at(1), n_units);
-    for (int w = 0; unit_at(w) < n_units && ok; ++w) {   // the producer alone may stop early
-      const Unit Un = unit_of(L, rec_next);
+    int4 rec_next = load_rec(seg, item_at(1) / ng, n_units);
+    for (int w = 0; item_at(w) < n_items && ok; ++w) {   // the producer alone may stop early
+      const Unit Un = unit_of(L, rec_next, item_at(w + 1) % ng);
       Gathered Gn;
       gather_issue<1>(seg, Un, lane, tok_lane, Gn);
-      rec_next = load_rec(seg, unit_at(w + 2), n_units);
+      rec_next = load_rec(seg, item_at(w + 2) / ng, n_units);
       if (slot_has_lora(G)) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -322,16 +339,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     const int mi = lane >> 3, ri = lane & 7;              // ldmatrix: matrix and row this lane addresses
     __nv_bfloat16* sb_hi = sb;
     __nv_bfloat16* sb_lo = sb + kUnitTok * kSbPitch;
-    int4 rec = load_rec(seg, unit_at(0), n_units);
+    int4 rec = load_rec(seg, item_at(0) / ng, n_units);
     Gathered G;
-    Unit U = unit_of(L, rec);
+    Unit U = unit_of(L, rec, item_at(0) % ng);
     gather_issue<4>(seg, U, lane, tok_store, G);
-    int4 rec_next = load_rec(seg, unit_at(1), n_units);
-    for (int w = 0; unit_at(w) < n_units; ++w) {
-      const Unit Un = unit_of(L, rec_next);
+    int4 rec_next = load_rec(seg, item_at(1) / ng, n_units);
+    for (int w = 0; item_at(w) < n_items; ++w) {
+      const Unit Un = unit_of(L, rec_next, item_at(w + 1) % ng);
       Gathered Gn;
       gather_issue<4>(seg, Un, lane, tok_store, Gn);
-      rec_next = load_rec(seg, unit_at(w + 2), n_units);
+      rec_next = load_rec(seg, item_at(w + 2) / ng, n_units);
       if (slot_has_lora(G)) {
         const uint64_t vm = valid_mask(G, U.r, L.num_pages, lane);
         const int ng = (U.r + 15) / 16;
@@ -467,7 +484,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   const int tk = G.tok[nt * 2 + (k & 1)];
-                  if (tk >= 0) L.delta[(int64_t)tk * H + fbase + mt * 16 + 8 * (k >> 1)] = e[mt][nt][k];
+                  if (tk >= 0) U.delta[(int64_t)tk * H + fbase + mt * 16 + 8 * (k >> 1)] = e[mt][nt][k];
                 }
             }
           }
@@ -521,7 +538,8 @@ int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
   }
   // Persistent clusters, as many as can be resident; each loops over the units.
   int groups = active_clusters();
-  if (L.seg->unit_cap < groups) groups = L.seg->unit_cap > 0 ? L.seg->unit_cap : 1;
+  const int item_cap = L.seg->unit_cap * L.n_group;
+  if (item_cap < groups) groups = item_cap > 0 ? item_cap : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * kCluster);
   cfg.blockDim = dim3(kThreads);

@@ -76,15 +76,20 @@ int launch_scatter_pages(const uint16_t* stage, const int32_t* d_pages, int64_t 
 int launch_segments_build(const lora_pool* pool, const int32_t* token_adapter, int32_t T,
                           const lora_segments* seg, cudaStream_t st, bool pdl);
 
+// One LoRA-delta launch covers n_group projection slots that read the same input x (the q, k
+// and v projections of a layer): every work unit is done once per slot, with that slot's page
+// table, into that slot's delta buffer.
 struct LoraLaunch {
   const uint16_t* pool;
   int64_t num_pages;
-  int32_t H, T, slot, n_slots;
+  int32_t H, T, n_slots;
+  int32_t n_group;                     // 1 .. LORA_MAX_GROUP
+  int32_t slot[LORA_MAX_GROUP];
+  float* delta[LORA_MAX_GROUP];        // [T][H] fp32 per slot of the group
   const int32_t* ptab;
   const int32_t* rank;
   const lora_segments* seg;
   const uint16_t* x;
-  float* delta;
   int32_t* err;
   bool pdl;
 };

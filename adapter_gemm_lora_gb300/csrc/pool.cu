@@ -414,7 +414,7 @@ struct SegLayout {
   size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials, total;
   int32_t max_seg, unit_cap;
 };
-SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
+SegLayout seg_layout(const lora_pool* p, int32_t T_max, int32_t max_group) {
   SegLayout L{};
   L.max_seg = std::min<int32_t>(T_max, p->max_adapters);
   L.unit_cap = T_max / kUnitTokens + L.max_seg + 1;
@@ -427,24 +427,28 @@ SegLayout seg_layout(const lora_pool* p, int32_t T_max) {
   L.tok_adapter = take((size_t)T_max * 4);
   L.units = take((size_t)L.unit_cap * 16);
   L.n_units = take(16);
-  L.delta = take((size_t)T_max * p->H * 4);
+  L.delta = take((size_t)max_group * T_max * p->H * 4);
   L.partials = take((size_t)gemm_partial_floats(T_max, p->H) * 4);
   L.total = off;
   return L;
 }
 }  // namespace
 
-int64_t lora_segments_size(const lora_pool* p, int32_t T_max) {
-  if (!p || T_max < 1 || T_max > LORA_MAX_TOKENS) return (int64_t)lora_fail(LORA_EINVAL, "lora_segments_size: bad arguments");
-  return (int64_t)seg_layout(p, T_max).total;
+int64_t lora_segments_size_group(const lora_pool* p, int32_t T_max, int32_t max_group) {
+  if (!p || T_max < 1 || T_max > LORA_MAX_TOKENS || max_group < 1 || max_group > LORA_MAX_GROUP)
+    return (int64_t)lora_fail(LORA_EINVAL, "lora_segments_size: bad arguments");
+  return (int64_t)seg_layout(p, T_max, max_group).total;
 }
 
-int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T_max, lora_segments* seg) {
-  if (!p || !ws || !seg || T_max < 1 || T_max > LORA_MAX_TOKENS)
+int64_t lora_segments_size(const lora_pool* p, int32_t T_max) { return lora_segments_size_group(p, T_max, 1); }
+
+int lora_segments_init_group(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T_max, int32_t max_group,
+                             lora_segments* seg) {
+  if (!p || !ws || !seg || T_max < 1 || T_max > LORA_MAX_TOKENS || max_group < 1 || max_group > LORA_MAX_GROUP)
     return lora_fail(LORA_EINVAL, "lora_segments_init: bad arguments");
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
     return lora_fail(LORA_EINVAL, "lora_segments_init: workspace must be 256-byte aligned");
-  const SegLayout L = seg_layout(p, T_max);
+  const SegLayout L = seg_layout(p, T_max, max_group);
   if (ws_bytes < (int64_t)L.total)
     return lora_fail(LORA_EINVAL, "lora_segments_init: workspace has " + std::to_string(ws_bytes) + " bytes, needs " +
                                       std::to_string(L.total));
@@ -461,10 +465,14 @@ int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T
   seg->units = reinterpret_cast<int32_t*>(b + L.units);
   seg->n_units = reinterpret_cast<int32_t*>(b + L.n_units);
   seg->unit_cap = L.unit_cap;
-  seg->reserved = 0;
+  seg->delta_slots = max_group;
   seg->delta = reinterpret_cast<float*>(b + L.delta);
   seg->gemm_partials = reinterpret_cast<float*>(b + L.partials);
   return LORA_OK;
+}
+
+int lora_segments_init(const lora_pool* p, void* ws, int64_t ws_bytes, int32_t T_max, lora_segments* seg) {
+  return lora_segments_init_group(p, ws, ws_bytes, T_max, 1, seg);
 }
 
 }  // extern "C"

@@ -2,8 +2,10 @@
 """Benchmark: tokens/s through the batched multi-LoRA projections, and roofline fraction.
 
 One step = one pass of the whole hot path over one batch: the segment build (tokens grouped
-by adapter) plus lora_linear_forward on every projection slot of the workload (LoRA delta:
-paged shrink and expand fused; tcgen05 base GEMM with the fused delta epilogue).  Adapters are resident
+by adapter) plus the forward of every projection slot of the workload (LoRA delta: paged
+shrink and expand fused; tcgen05 base GEMM with the fused delta epilogue), the q, k and v
+slots of a layer, which read the same input, in one lora_linear_forward_group call and o in
+one lora_linear_forward call.  Adapters are resident
 (loading is set-up, not timed).  Default workload: the decode batch (H=4096, q/k/v/o,
 256 requests x 1 token, 64 adapters of rank 8..64, Zipf(1.0) request->adapter, pool of
 2^18 pages half filled with KV pages).  Other workloads with --config 1..5.
@@ -157,12 +159,12 @@ def committed_traffic(kernel_file, config_key):
 # ------------------------------------------------------------------------------- workload bytes / flops
 def algorithmic(wl):
     """Algorithmic bytes and flops of one step (every slot), of one base-GEMM launch, and of one
-    LoRA-delta launch (slot average).
+    LoRA-delta launch (average over the step's launches: one per group of slots sharing x).
 
-    Base GEMM launch: W once, x once, y once.  LoRA-delta launch: the x rows of the tokens that
-    carry LoRA on the slot, every used adapter's A and B pages for the slot once, and the fp32
-    delta rows it writes.  The delta is an intermediate of this implementation's two-kernel
-    split; the step total does not count it.
+    Base GEMM launch: W once, x once, y once.  LoRA-delta launch over a group of slots that read
+    the same x: the x rows of the tokens that carry LoRA, once, then for every slot of the group
+    each used adapter's A and B pages once and the fp32 delta rows it writes.  The delta is an
+    intermediate of this implementation's two-kernel split; the step total does not count it.
     """
     H, T, S = wl.H, wl.T, wl.n_slots
     used = np.unique(wl.token_adapter[wl.token_adapter >= 0])
@@ -173,7 +175,9 @@ def algorithmic(wl):
     gemm_bytes = H * H * 2 + 2 * T * H * 2
     gemm_flops = 2 * T * H * H
     t_lora = int((wl.token_adapter >= 0).sum())
-    delta_bytes = t_lora * H * 2 + (lora_pages // S) * H * 2 + t_lora * H * 4
+    n_groups = len(wl.slot_groups())
+    delta_step = n_groups * t_lora * H * 2 + S * ((lora_pages // S) * H * 2 + t_lora * H * 4)
+    delta_bytes = delta_step // n_groups
     return dict(step_bytes=step_bytes, step_flops=step_flops, gemm_bytes=gemm_bytes, gemm_flops=gemm_flops,
                 delta_bytes=delta_bytes,
                 lora_page_bytes=lora_pages * H * 2, distinct_adapters=int(used.size), sum_rank=sum_r)
@@ -202,9 +206,12 @@ class Harness:
         self.W = [to_dev(wl.W(s)) for s in range(S)]
         self.y = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(S)]
         self.ta = torch.from_numpy(wl.token_adapter).to(device)
-        nbytes = L.lora_segments_size(self.pool, T)
+        # Per layer, q, k and v read the same input: one group call covers the three slots.
+        self.groups = wl.slot_groups()
+        max_group = max(len(g) for g in self.groups)
+        nbytes = L.lora_segments_size_group(self.pool, T, max_group)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.seg = L.lora_segments_init(self.pool, self.ws, nbytes, T)
+        self.seg = L.lora_segments_init_group(self.pool, self.ws, nbytes, T, max_group)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         # A step whose inputs are larger than the L2 evicts them itself: no flush is needed, and a
         # write-flush would leave dirty lines whose write-back lands inside the next timed step.
@@ -212,12 +219,20 @@ class Harness:
         self.flush = self.step_bytes <= L2_BYTES
         torch.cuda.synchronize()
 
-    def step(self, stream):
+    def forward_all(self, xs, stream):
+        """Every slot of the workload: one group call per run of slots sharing an input."""
         L, wl = self.L, self.wl
-        L.lora_segments_build(self.pool, self.ta, wl.T, self.seg, stream=stream)
-        for s in range(wl.n_slots):
-            L.lora_linear_forward(self.pool, self.seg, s, self.x[wl.slot_input(s)], self.W[s], self.y[s], None,
-                                  stream=stream)
+        for g in self.groups:
+            x = xs[wl.slot_input(g[0])]
+            if len(g) == 1:
+                L.lora_linear_forward(self.pool, self.seg, g[0], x, self.W[g[0]], self.y[g[0]], None, stream=stream)
+            else:
+                L.lora_linear_forward_group(self.pool, self.seg, g, x, [self.W[s] for s in g], [self.y[s] for s in g],
+                                            None, stream=stream)
+
+    def step(self, stream):
+        self.L.lora_segments_build(self.pool, self.ta, self.wl.T, self.seg, stream=stream)
+        self.forward_all(self.x, stream)
 
     def capture(self, n_steps, stream):
         """A graph of n_steps steps, each bracketed by events (and preceded by an L2 flush when the
@@ -331,9 +346,8 @@ class Harness:
                 for i in range(wl.n_inputs):
                     d_x[i].copy_(h_x[i], non_blocking=True)
                 L.lora_segments_build(self.pool, d_ta, T, self.seg, stream=stream.cuda_stream)
+                self.forward_all(d_x, stream.cuda_stream)
                 for s in range(S):
-                    L.lora_linear_forward(self.pool, self.seg, s, d_x[wl.slot_input(s)], self.W[s], self.y[s], None,
-                                          stream=stream.cuda_stream)
                     h_y[s].copy_(self.y[s], non_blocking=True)
                 e1.record()
                 e1.synchronize()

@@ -55,6 +55,7 @@ typedef struct CUstream_st* lora_stream_t;  /* identical to cudaStream_t */
 #define LORA_MAX_RANK      64
 #define LORA_MAX_ADAPTERS  16384    /* adapter ids are indices in [0, max_adapters) */
 #define LORA_MAX_TOKENS    65536    /* tokens per batch */
+#define LORA_MAX_GROUP     4        /* slots per lora_linear_forward_group call */
 
 typedef struct lora_pool lora_pool;
 
@@ -81,7 +82,8 @@ typedef struct lora_pool_stats_t {
  *                    perm[units[4u+2] .. units[4u+2] + units[4u+3]) (at most 16, all of one
  *                    segment) of adapter units[4u], whose rank is units[4u+1]; listed by
  *                    rank class (33..64, 17..32, 9..16, 1..8), then adapter id, then offset;
- * plus the fp32 scratch for the LoRA delta used by lora_linear_forward.  Calls that use
+ * plus the fp32 scratch for the LoRA delta used by lora_linear_forward (delta_slots
+ * buffers of [T_max][H], one per slot of a lora_linear_forward_group call).  Calls that use
  * the same workspace must be ordered on one stream: the scratch is reused by every
  * projection slot.
  */
@@ -98,8 +100,8 @@ typedef struct lora_segments {
   int32_t* units;         /* [4 * unit_cap] (adapter, rank, first perm index, tokens) */
   int32_t* n_units;
   int32_t unit_cap;
-  int32_t reserved;
-  float*   delta;         /* [T_max][H]  (x_t A) B (fp32) */
+  int32_t delta_slots;    /* fp32 delta buffers at `delta` (the workspace's max_group) */
+  float*   delta;         /* [delta_slots][T_max][H]  (x_t A) B (fp32) */
   float*   gemm_partials; /* [3][P][H] fp32 partial sums of the base GEMM for batches of <= 256
                              tokens (K split over 4 CTAs); P = min(T_max, 256) rounded up to 128 */
 } lora_segments;
@@ -159,6 +161,13 @@ int64_t lora_segments_size(const lora_pool* pool, int32_t T_max);
 int lora_segments_init(const lora_pool* pool, void* workspace_dev, int64_t workspace_bytes,
                        int32_t T_max, lora_segments* seg);
 
+/* The same for a workspace that also serves lora_linear_forward_group calls of up to
+ * max_group (1 .. LORA_MAX_GROUP) slots: it holds max_group delta buffers instead of one.
+ * lora_segments_size/init are these with max_group = 1. */
+int64_t lora_segments_size_group(const lora_pool* pool, int32_t T_max, int32_t max_group);
+int lora_segments_init_group(const lora_pool* pool, void* workspace_dev, int64_t workspace_bytes,
+                             int32_t T_max, int32_t max_group, lora_segments* seg);
+
 /*
  * Group a batch's tokens by adapter (stable: ascending adapter id, ties by token index).
  *   token_adapter  device int32 [T]: adapter id per token, -1 = no adapter;
@@ -186,6 +195,26 @@ int lora_segments_build(lora_pool* pool, const int32_t* token_adapter, int32_t T
 int lora_linear_forward(lora_pool* pool, const lora_segments* seg, int32_t slot,
                         const void* x, const void* W, void* y, float* delta_dbg,
                         lora_stream_t stream);
+
+/*
+ * n projection slots that read the same input x, e.g. the q, k and v projections of one layer
+ * ("S-LoRA, in depth", "The architecture": every layer's projections run over the whole
+ * batch; q, k and v all take the layer's hidden state).  Computes, for each i < n, exactly
+ * what lora_linear_forward(pool, seg, slots_host[i], x, W_host[i], y_host[i],
+ * delta_dbg_host[i], stream) computes, bit for bit, but the LoRA deltas of all n slots come
+ * from one kernel launch (its work list is every unit of the batch once per slot), followed
+ * by the n base GEMMs.
+ *   n               1 .. seg->delta_slots (see lora_segments_init_group);
+ *   slots_host      host int32 [n], distinct slots;
+ *   W_host, y_host  host arrays [n] of device pointers (W[out][in] bf16, y bf16 [T][H]); no y
+ *                   may alias x or another y;
+ *   delta_dbg_host  nullable host array [n] of nullable device fp32 [T][H] pointers.
+ * Errors: as lora_linear_forward; LORA_EINVAL also for n outside 1 .. seg->delta_slots or
+ * a repeated slot.
+ */
+int lora_linear_forward_group(lora_pool* pool, const lora_segments* seg, int32_t n, const int32_t* slots_host,
+                              const void* x, const void* const* W_host, void* const* y_host,
+                              float* const* delta_dbg_host, lora_stream_t stream);
 
 /* Synchronise `stream`, read and clear the device error word.  LORA_OK, or LORA_EDEVICE
  * with lora_last_error() naming the failed check (unknown adapter id, page id out of

@@ -85,13 +85,13 @@ class DeviceScene:
             self.tables[a] = mtab
         self.ws = None
 
-    def segments(self, token_adapter, stream=None):
+    def segments(self, token_adapter, stream=None, max_group=1):
         import torch
         T = len(token_adapter)
         T_max = max(T, 1)
-        nbytes = self.L.lora_segments_size(self.pool, T_max)
+        nbytes = self.L.lora_segments_size_group(self.pool, T_max, max_group)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        self.seg = self.L.lora_segments_init(self.pool, self.ws, nbytes, T_max)
+        self.seg = self.L.lora_segments_init_group(self.pool, self.ws, nbytes, T_max, max_group)
         self.ta_t = torch.from_numpy(np.asarray(token_adapter, dtype=np.int32)).cuda()
         self.L.lora_segments_build(self.pool, self.ta_t, T, self.seg, stream=stream)
         return self.seg
@@ -123,6 +123,15 @@ class DeviceScene:
         d = torch.empty((T, self.H), dtype=torch.float32, device="cuda") if with_delta else None
         self.L.lora_linear_forward(self.pool, self.seg, slot, x_t, W_t, y, d, stream=stream)
         return y, d
+
+    def forward_group(self, slots, x_t, W_ts, with_delta=True, stream=None):
+        """lora_linear_forward_group over `slots` (one shared x); returns lists of y and delta."""
+        import torch
+        T = x_t.shape[0]
+        ys = [torch.empty((T, self.H), dtype=torch.bfloat16, device="cuda") for _ in slots]
+        ds = [torch.empty((T, self.H), dtype=torch.float32, device="cuda") for _ in slots] if with_delta else None
+        self.L.lora_linear_forward_group(self.pool, self.seg, slots, x_t, W_ts, ys, ds, stream=stream)
+        return ys, ds
 
     def oracle(self, token_adapter, slot, x_bits, W_bits, tokens=None):
         return O.linear_forward(self.opool, self.tables, token_adapter, slot, x_bits, W_bits, tokens=tokens)

@@ -191,3 +191,23 @@ def test_device_calls_rejected_on_planning_pool(L):
     assert e.value.code == L.LORA_EINVAL
     assert L.lora_segments_size(pool, 100) > 100 * 64 * 4
     L.lora_pool_destroy(pool)
+
+
+def test_group_workspace_sizes_and_argument_checks(L):
+    """A group workspace holds one fp32 delta buffer per slot; bad group sizes are refused."""
+    H, T = 128, 300
+    pool = L.lora_pool_create(None, 10, H, 4, 1)
+    one = L.lora_segments_size(pool, T)
+    assert L.lora_segments_size_group(pool, T, 1) == one
+    for g in (2, 3, 4):
+        assert L.lora_segments_size_group(pool, T, g) - one == (g - 1) * T * H * 4
+    for g in (0, L.LORA_MAX_GROUP + 1):
+        with pytest.raises(L.LoraError) as e:
+            L.lora_segments_size_group(pool, T, g)
+        assert e.value.code == L.LORA_EINVAL
+    seg = L.lora_segments()
+    seg.delta_slots = 2
+    with pytest.raises(L.LoraError) as e:                 # planning pool: no device calls
+        L.lora_linear_forward_group(pool, seg, [0, 1], 16, [16, 16], [32, 48], stream=0)
+    assert e.value.code == L.LORA_EINVAL
+    L.lora_pool_destroy(pool)

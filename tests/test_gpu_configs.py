@@ -1,6 +1,7 @@
 """The five seeded workloads at full size, in the launch configuration the benchmark times
-(one segment build, then lora_linear_forward per projection slot), checked against the
-oracle on sampled outputs (GB300 only)."""
+(one segment build, then per layer one lora_linear_forward_group call for the q, k and v
+slots, which read the same input, and one lora_linear_forward call for o), checked against
+the oracle on sampled outputs (GB300 only)."""
 import numpy as np
 import pytest
 
@@ -43,23 +44,27 @@ def test_config_full_size(L, key, slots, n_tok):
     wl = workloads.make(key)
     check_slots = list(range(wl.n_slots)) if slots is None else slots
     sc = DeviceScene(L, wl, oracle_slots=set(check_slots), dense_oracle=False)
-    sc.segments(wl.token_adapter)
+    groups = wl.slot_groups()
+    sc.segments(wl.token_adapter, max_group=max(len(g) for g in groups))
     perm, off, sa = sc.read_segments()
     w = O.segments(wl.token_adapter)
     assert np.array_equal(perm, w[0]) and np.array_equal(off, w[1]) and np.array_equal(sa, w[2])
     tokens = None if n_tok is None else _sample_tokens(wl, n_tok, key)
-    xs = {}
     outs = {}
-    for slot in range(wl.n_slots):         # every slot runs, as in the timed step
-        i = wl.slot_input(slot)
-        if i not in xs:
-            xs = {i: (wl.x(i), None)}
-            xs[i] = (xs[i][0], bits_to_torch(xs[i][0]))
-        W_bits = wl.W(slot)
-        y, d = sc.forward(slot, xs[i][1], bits_to_torch(W_bits), with_delta=slot in check_slots)
-        if slot in check_slots:
-            outs[slot] = (torch_to_bits(y), d.cpu().numpy(), xs[i][0], W_bits)
-        del y, d
+    for group in groups:                   # every slot runs, as in the timed step
+        x_bits = wl.x(wl.slot_input(group[0]))
+        x_t = bits_to_torch(x_bits)
+        W_bits = [wl.W(slot) for slot in group]
+        checked = any(slot in check_slots for slot in group)
+        if len(group) > 1:
+            ys, ds = sc.forward_group(group, x_t, [bits_to_torch(b) for b in W_bits], with_delta=checked)
+        else:
+            y, d = sc.forward(group[0], x_t, bits_to_torch(W_bits[0]), with_delta=checked)
+            ys, ds = [y], [d]
+        for i, slot in enumerate(group):
+            if slot in check_slots:
+                outs[slot] = (torch_to_bits(ys[i]), ds[i].cpu().numpy(), x_bits, W_bits[i])
+        del ys, ds, x_t
     torch.cuda.synchronize()
     L.lora_status(sc.pool)
     for slot, (y_bits, d, x_bits, W_bits) in outs.items():

@@ -121,6 +121,65 @@ def test_small_parity(L, H, T, ranks, n_slots, none_share):
     sc.close()
 
 
+GROUP = [
+    # H, T, ranks, n_slots, none_share, slots of the group call
+    (256, 257, [8, 16, 32, 64, 1, 7], 4, 0.3, [2, 0, 3]),
+    (2048, 256, [64, 8, 16, 32, 1], 4, 0.2, [0, 1, 2]),      # decode shape: split-K base GEMM
+    (512, 33, [3, 64], 4, 0.0, [3, 1, 0, 2]),
+    (1024, 1, [16], 2, 0.0, [1]),
+    (384, 700, [8, 40, 64, 17], 3, 0.25, [1, 2]),            # several units per adapter
+]
+
+
+@pytest.mark.parametrize("H,T,ranks,n_slots,none_share,slots", GROUP)
+def test_group_forward_bitwise_equals_single_slot_calls(L, H, T, ranks, n_slots, none_share, slots):
+    """Slots that share x in one lora_linear_forward_group call give bit for bit what one
+    lora_linear_forward call per slot gives, and both meet the oracle's tolerance."""
+    wl = workloads.small(H=H, T=T, n_adapters=len(ranks), ranks=ranks, seed=7 * H + T, n_slots=n_slots,
+                         none_share=none_share)
+    present = (lambda a: [True] * (n_slots - 1) + [a % 2 == 0]) if n_slots > 1 else None
+    sc = DeviceScene(L, wl, present=present)
+    sc.segments(wl.token_adapter, max_group=len(slots))
+    x_bits = wl.x(0)
+    x_t = bits_to_torch(x_bits)
+    W_ts = [bits_to_torch(wl.W(s)) for s in slots]
+    for _ in range(2):                                    # the second call reuses the scratch
+        ys, ds = sc.forward_group(slots, x_t, W_ts)
+    for i, slot in enumerate(slots):
+        y1, d1 = sc.forward(slot, x_t, W_ts[i])
+        assert np.array_equal(torch_to_bits(ys[i]), torch_to_bits(y1)), f"slot {slot}: y differs from a single call"
+        assert np.array_equal(ds[i].cpu().numpy().view(np.uint32), d1.cpu().numpy().view(np.uint32)), \
+            f"slot {slot}: delta differs from a single call"
+        y_ref, d_ref = sc.oracle(wl.token_adapter, slot, x_bits, wl.W(slot))
+        check_close(torch_to_bits(ys[i]), ds[i].cpu().numpy(), y_ref, d_ref, f"group H={H} T={T} slot={slot}")
+    # without delta_dbg the deltas live in the workspace's scratch: same outputs
+    ys2, _ = sc.forward_group(slots, x_t, W_ts, with_delta=False)
+    for i in range(len(slots)):
+        assert np.array_equal(torch_to_bits(ys2[i]), torch_to_bits(ys[i]))
+    L.lora_status(sc.pool)
+    sc.close()
+
+
+def test_group_forward_argument_errors(L):
+    import torch
+    wl = workloads.small(H=64, T=4, n_adapters=1, ranks=[2], seed=83, n_slots=3)
+    sc = DeviceScene(L, wl)
+    sc.segments(wl.token_adapter, max_group=2)
+    x = bits_to_torch(wl.x(0))
+    W = bits_to_torch(wl.W(0))
+    y = [torch.empty_like(x) for _ in range(3)]
+    cases = [([0, 1, 2], [W] * 3, y),                    # more slots than the workspace's delta scratch
+             ([1, 1], [W] * 2, y[:2]),                    # a slot listed twice
+             ([0, 3], [W] * 2, y[:2]),                    # slot out of range
+             ([0, 1], [W] * 2, [y[0], y[0]]),             # two slots share one y
+             ([0, 1], [W] * 2, [y[0], x])]                # y aliases x
+    for slots, Ws, ys in cases:
+        with pytest.raises(L.LoraError) as e:
+            L.lora_linear_forward_group(sc.pool, sc.seg, slots, x, Ws, ys)
+        assert e.value.code == L.LORA_EINVAL, slots
+    sc.close()
+
+
 def test_config1_all_tokens(L):
     wl = workloads.make(1)
     sc = DeviceScene(L, wl)

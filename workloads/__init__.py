@@ -125,6 +125,16 @@ class Workload:
         layer, proj = divmod(slot, 4)
         return 2 * layer + (1 if proj == 3 else 0)
 
+    def slot_groups(self):
+        """Runs of consecutive slots that read the same input: [[q, k, v], [o], ...] per layer."""
+        groups = []
+        for slot in range(self.n_slots):
+            if groups and self.slot_input(groups[-1][-1]) == self.slot_input(slot):
+                groups[-1].append(slot)
+            else:
+                groups.append([slot])
+        return groups
+
     @property
     def n_inputs(self) -> int:
         return 1 if self.spec.n_slots == 1 else 2 * (self.spec.n_slots // 4)
