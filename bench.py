@@ -183,6 +183,23 @@ def algorithmic(wl):
                 lora_page_bytes=lora_pages * H * 2, distinct_adapters=int(used.size), sum_rank=sum_r)
 
 
+def gemm_kernel_name(H, T, n_sm):
+    """Which base-GEMM kernel the library launches for a batch (its tile choice, restated):
+    batches of <= 256 tokens split K over a cluster; larger ones walk their tiles with
+    persistent CTAs when there are more cluster tiles than clusters fit on the GPU."""
+    if T <= 256:
+        return "gemm_lora_kernel"
+    m_tiles = (H + 127) // 128
+    n_tiles = (T + 255) // 256
+    want = (3 * n_sm // 4 + m_tiles - 1) // m_tiles
+    if n_tiles < want:
+        n_tiles = min(want, (T + 31) // 32)
+    bn = min(256, ((T + n_tiles - 1) // n_tiles + 31) // 32 * 32)
+    n_tiles = (T + bn - 1) // bn
+    cn = 1 if bn < 128 else (4 if n_tiles % 4 == 0 else 2 if n_tiles % 2 == 0 else 1)
+    return "gemm_lora_persistent" if m_tiles * (n_tiles // cn) > n_sm // cn else "gemm_lora_kernel"
+
+
 # ------------------------------------------------------------------------------- our arm
 class Harness:
     def __init__(self, key, device):
@@ -395,7 +412,7 @@ def run_ours(args):
     launch_ms = per_launch_ms[dominant]
     if dominant == "gemm":
         kernel_file = os.path.join(ROOT, "adapter_gemm_lora_gb300", "csrc", "gemm_tcgen05.cu")
-        kernel_name = "gemm_lora_kernel"
+        kernel_name = gemm_kernel_name(wl.H, T, torch.cuda.get_device_properties(device).multi_processor_count)
         hbm_bound = alg["gemm_flops"] / alg["gemm_bytes"] < ridge
         alg_bytes, alg_flops = alg["gemm_bytes"], alg["gemm_flops"]
     else:
