@@ -5,7 +5,8 @@
 // W shared, A and B the token's own adapter.  Kernels on the caller's stream:
 //   1. LoRA delta: s = x A, then delta = s B, per run of tokens sharing an adapter (paged
 //      gathers, fused in one kernel; s stays on chip), for every slot of the call at once
-//   2. per slot, base GEMM x W^T on tcgen05, epilogue y = bf16_rne(acc + delta)
+//   2. base GEMM x W^T on tcgen05, epilogue y = bf16_rne(acc + delta): one launch per slot, or
+//      for a group of slots and a batch of <= 256 tokens one persistent launch over all of them
 #include <cuda_runtime.h>
 
 #include <string>
@@ -76,24 +77,30 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
   }
   if (rc != LORA_OK) return rc;
 
+  GemmLaunch G[LORA_MAX_GROUP];
   for (int i = 0; i < n; ++i) {
-    GemmLaunch G;
-    G.x = static_cast<const uint16_t*>(x);
-    G.W = static_cast<const uint16_t*>(W[i]);
-    G.y = static_cast<uint16_t*>(y[i]);
-    G.delta = L.delta[i];
-    G.tok_adapter = seg->tok_adapter;
-    G.ptab = p->d_ptab;
-    G.T = T;
-    G.H = H;
-    G.slot = slots[i];
-    G.n_slots = p->n_slots;
-    G.partials = seg->gemm_partials;
-    G.partials_floats = gemm_partial_floats(seg->T_max, H);
-    G.err = p->d_err;
-    G.pdl = !p->prof_on;
+    G[i].x = static_cast<const uint16_t*>(x);
+    G[i].W = static_cast<const uint16_t*>(W[i]);
+    G[i].y = static_cast<uint16_t*>(y[i]);
+    G[i].delta = L.delta[i];
+    G[i].tok_adapter = seg->tok_adapter;
+    G[i].ptab = p->d_ptab;
+    G[i].T = T;
+    G[i].H = H;
+    G[i].slot = slots[i];
+    G[i].n_slots = p->n_slots;
+    G[i].partials = seg->gemm_partials;
+    G[i].partials_floats = gemm_partial_floats(seg->T_max, H) * cap;
+    G[i].err = p->d_err;
+    G[i].pdl = !p->prof_on;
+  }
+  if (gemm_group_fits(G, n)) {          // decode-sized batch: one launch for every slot of the group
     ProfScope prof(p, LORA_KIND_GEMM, st);
-    rc = launch_gemm(G, st);
+    return launch_gemm_group(G, n, st);
+  }
+  for (int i = 0; i < n; ++i) {
+    ProfScope prof(p, LORA_KIND_GEMM, st);
+    rc = launch_gemm(G[i], st);
     if (rc != LORA_OK) return rc;
   }
   return LORA_OK;

@@ -201,6 +201,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with the
@@ -233,8 +242,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) { return __bfloat16_
 // Ballot masks of the tokens (columns) that carry LoRA on this slot, for the 32-column chunks
 // c0, c0 + step, ... (at most 4): all id loads are issued before any page-table load, so the two
 // dependent global reads cost one latency each for every chunk of the warp together.
-__device__ __forceinline__ void presence_masks(const GemmParams& p, int t_col0, int c0, int step, int c_end, int lane,
-                                               unsigned (&pm)[4]) {
+__device__ __forceinline__ void presence_masks(const GemmParams& p, int slot, int t_col0, int c0, int step, int c_end,
+                                               int lane, unsigned (&pm)[4]) {
   int a[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -245,7 +254,7 @@ __device__ __forceinline__ void presence_masks(const GemmParams& p, int t_col0, 
   int present[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    present[k] = a[k] >= 0 ? p.ptab[((int64_t)a[k] * p.n_slots + p.slot) * kTabStride] >= 0 : 0;
+    present[k] = a[k] >= 0 ? p.ptab[((int64_t)a[k] * p.n_slots + slot) * kTabStride] >= 0 : 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) pm[k] = __ballot_sync(0xffffffffu, present[k]);
 }
@@ -297,7 +306,7 @@ __device__ __forceinline__ void split_k_epilogue(const GemmParams& p, uint32_t t
     dv[i] = (c_first < c_end && t < p.T && feat < p.H) ? __ldg(p.delta + (size_t)t * p.H + feat) : 0.f;
   }
   unsigned pm[4];                                 // own chunks c_first + 2k
-  presence_masks(p, t0, c_first, 2, c_end, lane, pm);
+  presence_masks(p, p.slot, t0, c_first, 2, c_end, lane, pm);
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // all partials of the cluster
   if (!ok) return;
@@ -485,7 +494,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     tma_load_2d_plain(delta_s, &tm_d, m0, t0, bar_delta);
   }
   unsigned pm[4];                                 // chunks h + 2k
-  presence_masks(p, t0, h, 2, p.BN / 32, lane, pm);
+  presence_masks(p, p.slot, t0, h, 2, p.BN / 32, lane, pm);
   if (ok && !mbar_wait(bar_delta, 0)) {
     flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
     ok = false;
@@ -677,7 +686,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
       const int n_chunks = p.BN / 32;
       for (int c4 = 0; c4 < n_chunks; c4 += 4) {
         unsigned pm[4];
-        presence_masks(p, t0, c4, 1, n_chunks, lane, pm);
+        presence_masks(p, p.slot, t0, c4, 1, n_chunks, lane, pm);
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int c = c4 + k;
@@ -712,6 +721,285 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 2 * acc_cols);
   if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
+}
+
+// ---- grouped split-K variant (slots that share x, batches of <= 256 tokens) --------------
+// One launch serves the n slots of a lora_linear_forward_group call.  Its tiles are (slot,
+// feature tile) pairs of 128 features x all BN tokens, K split over a cluster of KS CTAs as in
+// gemm_lora_kernel, and persistent clusters walk the tiles.  Warp 0 streams the CTA's K slice
+// of W and x for tile after tile, warp 1 accumulates tile i in TMEM accumulator i % 2, and
+// warps 4-11 (two per TMEM lane quarter, each taking every other 16-column chunk) finish tile
+// i - 1 meanwhile: they write the partial sums of the other owners' token columns to the
+// tile's own scratch region, tell each of those owners through an mbarrier in its shared
+// memory (one remote arrive per warp, after a cluster-scope fence), wait until the peers have
+// done the same for their own columns (cluster-scope acquire), add the KS partials in
+// cluster-rank order, add the delta and write y.  So a tile's exchange and epilogue run under
+// the next tile's main loop, and the arithmetic is that of gemm_lora_kernel term for term:
+// each slot's y is bitwise the y of a single-slot call.
+constexpr int GROUP_THREADS = 384;
+struct GroupParams {
+  uint16_t* y[LORA_MAX_GROUP];
+  const float* delta[LORA_MAX_GROUP];
+  int32_t slot[LORA_MAX_GROUP];
+  int32_t m_tiles;                 // feature tiles per slot
+  int32_t n_tiles;                 // (slot, feature tile) pairs
+};
+
+// Arrive on the mbarrier at `local_bar`'s offset in CTA `rank` of the cluster, with cluster-scope
+// release: this thread's earlier writes, global memory included, are visible to any thread of
+// the cluster whose acquire wait observes the phase the arrival completes.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t local_bar, uint32_t rank) {
+  uint32_t rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+  const long long c0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    if (clock64() - c0 > kWaitLimitCycles) return false;
+  }
+}
+
+template <int KS>
+__global__ void __launch_bounds__(GROUP_THREADS, 1)
+gemm_lora_group_splitk(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                       const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_w3,
+                       const __grid_constant__ CUtensorMap tm_x, GemmParams p, GroupParams gp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGE_AREA);
+  // full[MAX_STAGES], empty[MAX_STAGES], tfull[2], tempty[2], ready[2], then the TMEM address
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 6);
+  const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * MAX_STAGES;
+  const uint32_t bar_tfull = bar_full + 16 * MAX_STAGES, bar_tempty = bar_tfull + 16, bar_ready = bar_tempty + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int me = (int)cluster_ctarank();                // this CTA's K slice and token-column owner rank
+  const int n_clusters = (int)gridDim.x / KS;
+  const int cluster_id = (int)blockIdx.x / KS;
+  const int stages = p.stages;
+  const int kc = p.kc;
+  const uint32_t xb = (uint32_t)(p.BN * BK * 2);
+  const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
+  const int kb0 = me * (p.n_kb / KS);
+  const int nk = p.n_kb / KS / kc;
+  const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
+  const int w = p.BN / KS;                              // token columns each CTA finishes
+  const size_t blk = (size_t)w * BM;                    // one partial block: w columns x 128 features
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 8);                 // one arrival per epilogue warp
+      mbar_init(bar_ready + 8 * b, (KS - 1) * 8);       // every epilogue warp of every peer
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 2 * acc_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();                                   // peers' barriers exist before any remote arrive
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {                                    // TMA producer, all tiles back to back
+      const uint64_t pol_w = policy_evict_first();      // each W tile is read once
+      const uint64_t pol_x = policy_evict_last();       // x is re-read by every tile
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tt = cluster_id; tt < gp.n_tiles && ok; tt += n_clusters) {
+        const int g = tt / gp.m_tiles;
+        const int m0 = (tt % gp.m_tiles) * BM;
+        const CUtensorMap* tw = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
+        for (int i = 0; i < nk; ++i, ++it) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1;
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+            flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * s, stage_bytes);
+          const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+          for (int c = 0; c < kc; ++c) {
+            const int kx = (kb0 + i * kc + c) * BK;
+            tma_load_2d(st + (uint32_t)c * A_BYTES, tw, kx, m0, bar_full + 8 * s, pol_w);
+            tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, 0, bar_full + 8 * s, pol_x);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {                                    // MMA issuer
+      const uint32_t idesc = make_idesc_bf16(BM, p.BN);
+      uint32_t it = 0;
+      int tile = 0;
+      bool ok = true;
+      for (int tt = cluster_id; tt < gp.n_tiles && ok; tt += n_clusters, ++tile) {
+        const int b = tile & 1;
+        if (!mbar_wait(bar_tempty + 8 * b, ((tile >> 1) & 1) ^ 1)) {   // accumulator b drained
+          flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)b * acc_cols;
+        for (int i = 0; i < nk; ++i, ++it) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1;
+          if (!mbar_wait(bar_full + 8 * s, ph)) {
+            flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+          for (int c = 0; c < kc; ++c) {
+            const uint64_t ad = sw128_kmajor_desc(st + (uint32_t)c * A_BYTES);
+            const uint64_t bd = sw128_kmajor_desc(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16_ss(acc, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
+          }
+          mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) mma_commit(bar_tfull + 8 * b);            // accumulator b complete
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- epilogue warps: TMEM lane quarter q, 16-column chunks u with u % 2 == h ----
+    const int q = warp & 3, h = (warp - 4) >> 2;
+    const int row = q * 32 + lane;
+    pdl_wait_then_release();      // the delta and ids come from earlier kernels, as do the scratch's last readers
+    int tile = 0;
+    for (int tt = cluster_id; tt < gp.n_tiles; tt += n_clusters, ++tile) {
+      const int b = tile & 1;
+      const uint32_t ph = (tile >> 1) & 1;
+      const int g = tt / gp.m_tiles;
+      const int feat = (tt % gp.m_tiles) * BM + row;    // this thread's output feature
+      int slot = gp.slot[0];
+      uint16_t* y = gp.y[0];
+      const float* delta = gp.delta[0];
+#pragma unroll
+      for (int k = 1; k < LORA_MAX_GROUP; ++k)
+        if (g == k) {
+          slot = gp.slot[k];
+          y = gp.y[k];
+          delta = gp.delta[k];
+        }
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * b, ph));
+      if (!ok) {
+        if (lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc_row = tmem + (uint32_t)b * acc_cols + ((uint32_t)(q * 32) << 16);
+      // The tile's scratch region: block (owner o, sender s) at o * (KS - 1) + (s < o ? s : s - 1).
+      float* scratch = p.partials + (size_t)tt * KS * (KS - 1) * blk;
+      // 1. this CTA's partial sums of the other owners' columns
+      for (int u = h; u < p.BN / 16; u += 2) {
+        const int o = (u * 16) / w;
+        if (o == me) continue;
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(acc_row + (uint32_t)(u * 16), v);
+        tmem_ld_wait();
+        float* dst = scratch + (size_t)(o * (KS - 1) + (me < o ? me : me - 1)) * blk + (size_t)(u * 16 - o * w) * BM + row;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[(size_t)i * BM] = __uint_as_float(v[i]);
+      }
+      // 2. each of those owners learns that this warp's share of its columns is written: the
+      //    warp barrier orders the lanes' stores before lane 0's cluster-scope fence and arrives
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+#pragma unroll
+        for (int o = 0; o < KS; ++o)
+          if (o != me) mbar_arrive_remote_release(bar_ready + 8 * b, (uint32_t)o);
+      }
+      __syncwarp();
+      // 3. own columns [me * w, (me + 1) * w): wait for the peers' partials, add the KS partials
+      //    in cluster-rank order, add the delta, write y
+      ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar_ready + 8 * b, ph));
+      if (!ok) {
+        if (lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+        break;
+      }
+#pragma unroll 1
+      for (int u = me * (w / 16) + h; u < (me + 1) * (w / 16); u += 2) {
+        const int tc = u * 16;
+        // tokens of this chunk that carry LoRA on the slot (one ballot over the 32-token chunk)
+        int a = -1;
+        const int tl = (tc & ~31) + lane;
+        if (tl < p.T) a = p.tok_adapter[tl];
+        const int present = a >= 0 ? p.ptab[((int64_t)a * p.n_slots + slot) * kTabStride] >= 0 : 0;
+        const unsigned pmask = __ballot_sync(0xffffffffu, present) >> (tc & 16);
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(acc_row + (uint32_t)tc, v);
+        tmem_ld_wait();
+        float dv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          dv[i] = (((pmask >> i) & 1u) && tc + i < p.T && feat < p.H) ? __ldg(delta + (size_t)(tc + i) * p.H + feat) : 0.f;
+        const float* in0 = scratch + (size_t)(me * (KS - 1)) * blk + (size_t)(tc - me * w) * BM + row;
+        float pv[KS - 1][16];
+#pragma unroll
+        for (int j = 0; j < KS - 1; ++j)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pv[j][i] = __ldcg(in0 + (size_t)j * blk + (size_t)i * BM);
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = me == 0 ? __uint_as_float(v[i]) : pv[0][i];
+#pragma unroll
+        for (int src = 1; src < KS; ++src) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float peer = src < me ? pv[src < KS - 1 ? src : KS - 2][i] : pv[src - 1][i];
+            acc[i] += src == me ? __uint_as_float(v[i]) : peer;
+          }
+        }
+        if (feat < p.H) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (tc + i < p.T) y[(size_t)(tc + i) * p.H + feat] = f32_to_bf16_rn((pmask >> i) & 1u ? acc[i] + dv[i] : acc[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);   // accumulator b may be overwritten
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 2 * acc_cols);
+  cluster_sync_all();                             // no peer may still arrive on this CTA's barriers
 }
 
 // ---- host side --------------------------------------------------------------------------
@@ -914,4 +1202,137 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, P);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_kernel launch");
+}
+
+namespace {
+// Split-K geometry of a batch of <= 256 tokens, as launch_gemm chooses it.
+struct SplitK {
+  int ks, bn, kc, stages;
+};
+bool split_k_geometry(int T, int H, SplitK& g) {
+  const int n_kb = H / BK;
+  if (T > MAX_BN || n_kb % 2 != 0) return false;
+  g.ks = n_kb % 4 == 0 ? 4 : 2;
+  g.bn = ((T + 32 * g.ks - 1) / (32 * g.ks)) * (32 * g.ks);
+  const int kb_cta = n_kb / g.ks;
+  const int chunk_bytes = A_BYTES + g.bn * BK * 2;
+  g.kc = 1;
+  while (g.bn < 128 && g.kc < 4 && 2 * g.kc * chunk_bytes <= 96 * 1024 && kb_cta % (2 * g.kc) == 0) g.kc *= 2;
+  g.stages = STAGE_AREA / (g.kc * chunk_bytes);
+  if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
+  return true;
+}
+
+template <int KS>
+int group_clusters() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(KS * 64);
+  cfg.blockDim = dim3(GROUP_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_lora_group_splitk<KS>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = device_sm_count() / KS;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <int KS>
+int launch_group_ks(const GemmLaunch* G, int n, const SplitK& sk, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_lora_group_splitk<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return lora_cuda_fail(e, "gemm group kernel attribute");
+    attr_set[dev] = true;
+  }
+  const int H = G[0].H, T = G[0].T;
+  const int m_tiles = (H + BM - 1) / BM;
+  CUtensorMap tm_w[LORA_MAX_GROUP], tm_x;
+  for (int i = 0; i < n; ++i) {
+    int rc = encode_2d(&tm_w[i], G[i].W, (uint64_t)H, (uint64_t)H, (uint32_t)BM);
+    if (rc != LORA_OK) return rc;
+  }
+  for (int i = n; i < LORA_MAX_GROUP; ++i) tm_w[i] = tm_w[0];
+  int rc = encode_2d(&tm_x, G[0].x, (uint64_t)H, (uint64_t)T, (uint32_t)sk.bn);
+  if (rc != LORA_OK) return rc;
+  GemmParams P;
+  P.y = G[0].y;
+  P.delta = G[0].delta;
+  P.partials = G[0].partials;
+  P.tok_adapter = G[0].tok_adapter;
+  P.ptab = G[0].ptab;
+  P.err = G[0].err;
+  P.T = T;
+  P.H = H;
+  P.BN = sk.bn;
+  P.n_kb = H / BK;
+  P.kc = sk.kc;
+  P.stages = sk.stages;
+  P.cn = 1;
+  P.ks = KS;
+  P.slot = G[0].slot;
+  P.n_slots = G[0].n_slots;
+  GroupParams gp = {};
+  for (int i = 0; i < LORA_MAX_GROUP; ++i) {
+    const int j = i < n ? i : 0;
+    gp.y[i] = G[j].y;
+    gp.delta[i] = G[j].delta;
+    gp.slot[i] = G[j].slot;
+  }
+  gp.m_tiles = m_tiles;
+  gp.n_tiles = n * m_tiles;
+  int clusters = group_clusters<KS>();
+  if (clusters > gp.n_tiles) clusters = gp.n_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * KS);
+  cfg.blockDim = dim3(GROUP_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = KS;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = G[0].pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_group_splitk<KS>, tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, P, gp);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_group_splitk launch");
+}
+}  // namespace
+
+bool gemm_group_fits(const GemmLaunch* G, int n) {
+  if (n < 2 || n > LORA_MAX_GROUP) return false;
+  SplitK sk;
+  if (!split_k_geometry(G[0].T, G[0].H, sk)) return false;
+  for (int i = 1; i < n; ++i)
+    if (G[i].x != G[0].x || G[i].T != G[0].T || G[i].H != G[0].H || G[i].partials != G[0].partials) return false;
+  const int m_tiles = (G[0].H + BM - 1) / BM;
+  return G[0].partials && (int64_t)n * (sk.ks - 1) * sk.bn * m_tiles * BM <= G[0].partials_floats;
+}
+
+int launch_gemm_group(const GemmLaunch* G, int n, cudaStream_t st) {
+  SplitK sk;
+  if (!gemm_group_fits(G, n) || !split_k_geometry(G[0].T, G[0].H, sk))
+    return lora_fail(LORA_EINVAL, "launch_gemm_group: the group does not fit the split-K kernel");
+  return sk.ks == 4 ? launch_group_ks<4>(G, n, sk, st) : launch_group_ks<2>(G, n, sk, st);
 }

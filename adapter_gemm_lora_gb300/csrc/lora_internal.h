@@ -109,6 +109,11 @@ struct GemmLaunch {
   bool pdl;
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
+// n (2 .. LORA_MAX_GROUP) slots that read the same x, batches of <= 256 tokens: one persistent
+// split-K launch over every (slot, feature tile).  gemm_group_fits says whether the group
+// qualifies (split-K geometry, one x, scratch for n slots); otherwise launch_gemm per slot.
+bool gemm_group_fits(const GemmLaunch* G, int n);
+int launch_gemm_group(const GemmLaunch* G, int n, cudaStream_t st);
 // Capacity of the base GEMM's split-K scratch for a workspace of T_max tokens: 3 partial tiles
 // (4-way split) of up to 256 token columns, the tile rounded up to 128 columns.
 inline int64_t gemm_partial_floats(int32_t T_max, int32_t H) {

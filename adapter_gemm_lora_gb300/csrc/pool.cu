@@ -428,7 +428,7 @@ SegLayout seg_layout(const lora_pool* p, int32_t T_max, int32_t max_group) {
   L.units = take((size_t)L.unit_cap * 16);
   L.n_units = take(16);
   L.delta = take((size_t)max_group * T_max * p->H * 4);
-  L.partials = take((size_t)gemm_partial_floats(T_max, p->H) * 4);
+  L.partials = take((size_t)max_group * gemm_partial_floats(T_max, p->H) * 4);
   L.total = off;
   return L;
 }

@@ -102,8 +102,9 @@ typedef struct lora_segments {
   int32_t unit_cap;
   int32_t delta_slots;    /* fp32 delta buffers at `delta` (the workspace's max_group) */
   float*   delta;         /* [delta_slots][T_max][H]  (x_t A) B (fp32) */
-  float*   gemm_partials; /* [3][P][H] fp32 partial sums of the base GEMM for batches of <= 256
-                             tokens (K split over 4 CTAs); P = min(T_max, 256) rounded up to 128 */
+  float*   gemm_partials; /* [delta_slots][3][P][H] fp32 partial sums of the base GEMM for batches
+                             of <= 256 tokens (K split over 4 CTAs); P = min(T_max, 256) rounded
+                             up to 128 */
 } lora_segments;
 
 /*
@@ -162,8 +163,8 @@ int lora_segments_init(const lora_pool* pool, void* workspace_dev, int64_t works
                        int32_t T_max, lora_segments* seg);
 
 /* The same for a workspace that also serves lora_linear_forward_group calls of up to
- * max_group (1 .. LORA_MAX_GROUP) slots: it holds max_group delta buffers instead of one.
- * lora_segments_size/init are these with max_group = 1. */
+ * max_group (1 .. LORA_MAX_GROUP) slots: it holds max_group delta buffers and max_group
+ * split-K scratch areas instead of one.  lora_segments_size/init are these with max_group = 1. */
 int64_t lora_segments_size_group(const lora_pool* pool, int32_t T_max, int32_t max_group);
 int lora_segments_init_group(const lora_pool* pool, void* workspace_dev, int64_t workspace_bytes,
                              int32_t T_max, int32_t max_group, lora_segments* seg);

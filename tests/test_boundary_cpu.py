@@ -194,13 +194,15 @@ def test_device_calls_rejected_on_planning_pool(L):
 
 
 def test_group_workspace_sizes_and_argument_checks(L):
-    """A group workspace holds one fp32 delta buffer per slot; bad group sizes are refused."""
+    """A group workspace holds one fp32 delta buffer and one split-K scratch area per slot; bad
+    group sizes are refused."""
     H, T = 128, 300
     pool = L.lora_pool_create(None, 10, H, 4, 1)
     one = L.lora_segments_size(pool, T)
     assert L.lora_segments_size_group(pool, T, 1) == one
+    per_slot = T * H * 4 + 3 * 256 * H * 4           # fp32 delta + split-K scratch (3 tiles of 256 tokens)
     for g in (2, 3, 4):
-        assert L.lora_segments_size_group(pool, T, g) - one == (g - 1) * T * H * 4
+        assert L.lora_segments_size_group(pool, T, g) - one == (g - 1) * per_slot
     for g in (0, L.LORA_MAX_GROUP + 1):
         with pytest.raises(L.LoraError) as e:
             L.lora_segments_size_group(pool, T, g)
