@@ -157,14 +157,28 @@ def committed_traffic(kernel_file, config_key):
 
 
 # ------------------------------------------------------------------------------- workload bytes / flops
-def algorithmic(wl):
-    """Algorithmic bytes and flops of one step (every slot), of one base-GEMM launch, and of one
-    LoRA-delta launch (average over the step's launches: one per group of slots sharing x).
+def gemm_launch_groups(wl):
+    """The slots each base-GEMM launch of a step covers (the library's rule, restated): a group
+    call on a batch of <= 256 tokens whose K splits evenly runs one grouped launch; otherwise
+    every slot has its own launch."""
+    out = []
+    for g in wl.slot_groups():
+        if len(g) > 1 and wl.T <= 256 and (wl.H // 64) % 2 == 0:
+            out.append(g)
+        else:
+            out += [[s] for s in g]
+    return out
 
-    Base GEMM launch: W once, x once, y once.  LoRA-delta launch over a group of slots that read
-    the same x: the x rows of the tokens that carry LoRA, once, then for every slot of the group
-    each used adapter's A and B pages once and the fp32 delta rows it writes.  The delta is an
-    intermediate of this implementation's two-kernel split; the step total does not count it.
+
+def algorithmic(wl):
+    """Algorithmic bytes and flops of one step (every slot), and of one base-GEMM and one
+    LoRA-delta launch (averages over the step's launches of each kind).
+
+    Base GEMM launch: W of each of its slots once, x once, y of each slot once.  LoRA-delta
+    launch over a group of slots that read the same x: the x rows of the tokens that carry LoRA,
+    once, then for every slot of the group each used adapter's A and B pages once and the fp32
+    delta rows it writes.  The delta is an intermediate of this implementation's two-kernel
+    split; the step total does not count it.
     """
     H, T, S = wl.H, wl.T, wl.n_slots
     used = np.unique(wl.token_adapter[wl.token_adapter >= 0])
@@ -172,8 +186,9 @@ def algorithmic(wl):
     sum_r = int(wl.ranks[wl.token_adapter[wl.token_adapter >= 0]].astype(np.int64).sum())
     step_bytes = S * H * H * 2 + wl.n_inputs * T * H * 2 + S * T * H * 2 + lora_pages * H * 2
     step_flops = S * (2 * T * H * H + 4 * H * sum_r)
-    gemm_bytes = H * H * 2 + 2 * T * H * 2
-    gemm_flops = 2 * T * H * H
+    launches = gemm_launch_groups(wl)
+    gemm_bytes = sum(len(g) * (H * H * 2 + T * H * 2) + T * H * 2 for g in launches) // len(launches)
+    gemm_flops = S * 2 * T * H * H // len(launches)
     t_lora = int((wl.token_adapter >= 0).sum())
     n_groups = len(wl.slot_groups())
     delta_step = n_groups * t_lora * H * 2 + S * ((lora_pages // S) * H * 2 + t_lora * H * 4)
@@ -183,8 +198,19 @@ def algorithmic(wl):
                 lora_page_bytes=lora_pages * H * 2, distinct_adapters=int(used.size), sum_rank=sum_r)
 
 
+def gemm_kernel_names(wl, n_sm):
+    """The base-GEMM kernels of a step, one name per distinct kernel ("a + b")."""
+    names = []
+    for g in gemm_launch_groups(wl):
+        k = (f"gemm_lora_group_splitk<{4 if (wl.H // 64) % 4 == 0 else 2}>" if len(g) > 1
+             else gemm_kernel_name(wl.H, wl.T, n_sm))
+        if k not in names:
+            names.append(k)
+    return " + ".join(names)
+
+
 def gemm_kernel_name(H, T, n_sm):
-    """Which base-GEMM kernel the library launches for a batch (its tile choice, restated):
+    """Which base-GEMM kernel the library launches for one slot (its tile choice, restated):
     batches of <= 256 tokens split K over a cluster; larger ones walk their tiles with
     persistent CTAs when there are more cluster tiles than clusters fit on the GPU."""
     if T <= 256:
@@ -405,14 +431,16 @@ def run_ours(args):
     ms_per_step = total_ms_max / steps
     per_launch_ms = {k: res["kern_ms"][k] / max(1, res["launches_per_graph"][k]) for k in ("gemm", "delta")}
     shares = {k: v / max(1e-12, sum(res["kern_ms"].values())) for k, v in res["kern_ms"].items()}
-    # The roofline object describes the kernel with the largest share of device time: the base
-    # GEMM (its roof follows the workload's arithmetic intensity) or the LoRA delta (HBM).
+    # The roofline object describes the kernel kind with the largest share of device time: the
+    # base GEMM (its roof follows the workload's arithmetic intensity) or the LoRA delta (HBM).
+    # A kind may run as two kernels in one step (a grouped launch for q/k/v, a single one for o):
+    # its figures are then per-launch averages, algorithmic bytes and time alike.
     dominant = "delta" if res["kern_ms"]["delta"] > res["kern_ms"]["gemm"] else "gemm"
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     launch_ms = per_launch_ms[dominant]
     if dominant == "gemm":
         kernel_file = os.path.join(ROOT, "adapter_gemm_lora_gb300", "csrc", "gemm_tcgen05.cu")
-        kernel_name = gemm_kernel_name(wl.H, T, torch.cuda.get_device_properties(device).multi_processor_count)
+        kernel_name = gemm_kernel_names(wl, torch.cuda.get_device_properties(device).multi_processor_count)
         hbm_bound = alg["gemm_flops"] / alg["gemm_bytes"] < ridge
         alg_bytes, alg_flops = alg["gemm_bytes"], alg["gemm_flops"]
     else:

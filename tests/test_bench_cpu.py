@@ -20,8 +20,10 @@ def test_algorithmic_model_config2():
     wl = workloads.make(2)
     a = bench.algorithmic(wl)
     H, T = 4096, 256
-    assert a["gemm_bytes"] == H * H * 2 + 2 * T * H * 2
-    assert a["gemm_flops"] == 2 * T * H * H
+    # base GEMM: one grouped launch for q/k/v (x read once) and one for o, per step
+    assert bench.gemm_launch_groups(wl) == [[0, 1, 2], [3]]
+    assert a["gemm_bytes"] == (4 * H * H * 2 + 2 * T * H * 2 + 4 * T * H * 2) // 2
+    assert a["gemm_flops"] == 4 * 2 * T * H * H // 2
     w_bytes = 4 * H * H * 2
     # resident adapters used by the batch, A and B once per slot
     used = np.unique(wl.token_adapter)
@@ -36,6 +38,7 @@ def test_algorithmic_model_config2():
 def test_algorithmic_prefill_is_tensor_bound():
     wl = workloads.make(3)
     a = bench.algorithmic(wl)
+    assert bench.gemm_launch_groups(wl) == [[0], [1], [2], [3]]      # 9,553 tokens: one launch per slot
     pk = bench.load_peaks()
     assert a["step_flops"] / a["step_bytes"] > pk["bf16_tflops"] * 1e3 / pk["hbm_gbs"]
 
