@@ -29,6 +29,7 @@ LORA_ERANK = -4
 LORA_EEXIST = -5
 LORA_ECUDA = -6
 LORA_EDEVICE = -7
+LORA_EBUSY = -8
 LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 16384
 LORA_MAX_TOKENS = 65536
@@ -40,7 +41,9 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",
             "lora_linear_forward", "lora_status", "lora_pool_stats", "lora_last_error", "lora_pool_destroy",
             "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc",
-            "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group"]
+            "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group",
+            "lora_adapter_acquire", "lora_adapter_release", "lora_adapter_refs", "lora_pool_evict_idle",
+            "lora_adapter_ensure"]
 KINDS = ("segments", "delta", "gemm", "scatter")
 
 
@@ -97,6 +100,11 @@ def _load():
         "lora_segments_size_group": (I64, [VP, I32, I32]),
         "lora_segments_init_group": (I32, [VP, VP, I64, I32, I32, P(lora_segments)]),
         "lora_linear_forward_group": (I32, [VP, P(lora_segments), I32, VP, VP, VP, VP, VP, VP]),
+        "lora_adapter_acquire": (I32, [VP, I32]),
+        "lora_adapter_release": (I32, [VP, I32]),
+        "lora_adapter_refs": (I32, [VP, I32]),
+        "lora_pool_evict_idle": (I32, [VP, I64, VP, VP, VP]),
+        "lora_adapter_ensure": (I32, [VP, I32, I32, VP, VP, VP, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -192,6 +200,56 @@ def lora_adapter_load(pool, adapter_id: int, rank: int, A_host: Optional[Sequenc
 
 def lora_adapter_unload(pool, adapter_id: int, stream=None, planning: bool = False) -> None:
     _check(_load().lora_adapter_unload(pool, adapter_id, 0 if planning else _stream(stream)))
+
+
+def lora_adapter_acquire(pool, adapter_id: int) -> None:
+    _check(_load().lora_adapter_acquire(pool, adapter_id))
+
+
+def lora_adapter_release(pool, adapter_id: int) -> None:
+    _check(_load().lora_adapter_release(pool, adapter_id))
+
+
+def lora_adapter_refs(pool, adapter_id: int) -> int:
+    """Active requests of a resident adapter, -1 if it is not resident."""
+    return int(_load().lora_adapter_refs(pool, adapter_id))
+
+
+def lora_pool_evict_idle(pool, need: int, max_adapters: int, stream=None, planning: bool = False) -> list:
+    """Evict idle adapters (earliest load first) until `need` pages are free; returns their ids."""
+    ev = np.zeros(max(max_adapters, 1), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(_load().lora_pool_evict_idle(pool, need, 0 if planning else _stream(stream), _ptr(ev), ctypes.byref(n)))
+    return ev[:n.value].tolist()
+
+
+def lora_adapter_ensure(pool, adapter_id: int, rank: int, A_host: Optional[Sequence], B_host: Optional[Sequence],
+                        n_slots: int, max_adapters: int, stream=None, planning: bool = False):
+    """Make an adapter resident with one more active request (loading it, after evicting idle
+    adapters, if needed).  Returns (page table int32 [n_slots, 2, rank], loaded, evicted ids)."""
+    keep = []
+
+    def arr(seq):
+        if seq is None:
+            return None
+        a = (ctypes.c_void_p * n_slots)()
+        for i, m in enumerate(seq):
+            if m is not None:
+                m = np.ascontiguousarray(m, dtype=np.uint16)
+                keep.append(m)
+                a[i] = m.ctypes.data
+        return a
+
+    a_arr, b_arr = arr(A_host), arr(B_host)
+    table = np.zeros((n_slots, 2, max(rank, 1)), dtype=np.int32)
+    loaded = ctypes.c_int32(0)
+    ev = np.zeros(max(max_adapters, 1), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    st = 0 if planning else _stream(stream)
+    _check(_load().lora_adapter_ensure(pool, adapter_id, rank, ctypes.cast(a_arr, ctypes.c_void_p) if a_arr else None,
+                                       ctypes.cast(b_arr, ctypes.c_void_p) if b_arr else None, st, _ptr(table),
+                                       ctypes.byref(loaded), _ptr(ev), ctypes.byref(n)))
+    return table, bool(loaded.value), ev[:n.value].tolist()
 
 
 def lora_segments_size(pool, T_max: int) -> int:

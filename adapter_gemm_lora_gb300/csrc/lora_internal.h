@@ -35,6 +35,9 @@ struct lora_pool {
   std::vector<uint8_t> page_state;                // 0 free, 1 reserved, 2 adapter
   std::vector<int32_t> rank;                      // per adapter id; 0 = not loaded
   std::vector<std::vector<int32_t>> tables;       // per adapter id: [n_slots][2][rank]
+  std::vector<int32_t> refs;                      // per adapter id: active requests
+  std::vector<int64_t> load_seq;                  // per adapter id: order of its load (eviction order)
+  int64_t next_seq = 0;
   int64_t adapter_pages = 0;
   int64_t reserved_pages = 0;
   int32_t resident = 0;

@@ -186,6 +186,8 @@ int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slo
   }
   p->rank.assign(max_adapters, 0);
   p->tables.resize(max_adapters);
+  p->refs.assign(max_adapters, 0);
+  p->load_seq.assign(max_adapters, 0);
 
   if (!p->planning) {
     cudaError_t e = cudaGetDevice(&p->device);
@@ -347,6 +349,8 @@ int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const
   }
   for (int32_t pg : taken) p->page_state[pg] = 2;
   p->rank[aid] = rank;
+  p->refs[aid] = 0;
+  p->load_seq[aid] = p->next_seq++;
   p->tables[aid] = table;
   p->adapter_pages += need;
   p->resident += 1;
@@ -354,16 +358,18 @@ int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const
   return LORA_OK;
 }
 
-int lora_adapter_unload(lora_pool* p, int32_t aid, lora_stream_t stream) {
-  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_unload: pool is NULL");
-  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
-    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_unload: adapter " + std::to_string(aid) + " is not loaded");
+}  // extern "C"
+
+namespace {
+// Clear a resident adapter's device page table and rank (in `stream` order) and give its pages
+// back to the free list in the order they were taken.
+int drop_adapter(lora_pool* p, int32_t aid, lora_stream_t stream, const char* who) {
   if (!p->planning) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(p->d_ptab + (size_t)aid * p->n_slots * kTabStride, 0xFF,
                                     (size_t)p->n_slots * kTabStride * sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_rank + aid, 0, sizeof(int32_t), st);
-    if (e != cudaSuccess) return lora_cuda_fail(e, "lora_adapter_unload");
+    if (e != cudaSuccess) return lora_cuda_fail(e, who);
   }
   int64_t n = 0;
   for (int32_t pg : p->tables[aid]) {
@@ -374,8 +380,122 @@ int lora_adapter_unload(lora_pool* p, int32_t aid, lora_stream_t stream) {
   }
   p->adapter_pages -= n;
   p->rank[aid] = 0;
+  p->refs[aid] = 0;
   p->tables[aid].clear();
   p->resident -= 1;
+  return LORA_OK;
+}
+
+int64_t adapter_page_count(const lora_pool* p, int32_t aid) {
+  int64_t n = 0;
+  for (int32_t pg : p->tables[aid]) n += pg >= 0;
+  return n;
+}
+
+// Idle resident adapters in eviction order (earliest load first) and how many of them must go
+// for `need` pages to be free; -1 if all of them would not be enough.
+int evict_plan(const lora_pool* p, int64_t need, std::vector<int32_t>& order) {
+  order.clear();
+  for (int32_t a = 0; a < p->max_adapters; ++a)
+    if (p->rank[a] != 0 && p->refs[a] == 0) order.push_back(a);
+  std::sort(order.begin(), order.end(), [p](int32_t a, int32_t b) { return p->load_seq[a] < p->load_seq[b]; });
+  int64_t free_pages = (int64_t)p->free_list.size();
+  int k = 0;
+  while (free_pages < need && k < (int)order.size()) free_pages += adapter_page_count(p, order[k++]);
+  return free_pages >= need ? k : -1;
+}
+
+int evict_idle(lora_pool* p, int64_t need, lora_stream_t stream, int32_t* evicted_host, int32_t* n_evicted,
+               const char* who) {
+  if (n_evicted) *n_evicted = 0;
+  std::vector<int32_t> order;
+  const int k = evict_plan(p, need, order);
+  if (k < 0)
+    return lora_fail(LORA_ENOPAGES, std::string(who) + ": " + std::to_string(need) + " pages needed, " +
+                                        std::to_string(p->free_list.size()) + " free and idle adapters hold too few");
+  for (int i = 0; i < k; ++i) {
+    const int rc = drop_adapter(p, order[i], stream, who);
+    if (rc != LORA_OK) return rc;
+    if (evicted_host) evicted_host[i] = order[i];
+    if (n_evicted) *n_evicted = i + 1;
+  }
+  return LORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int lora_adapter_unload(lora_pool* p, int32_t aid, lora_stream_t stream) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_unload: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
+    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_unload: adapter " + std::to_string(aid) + " is not loaded");
+  if (p->refs[aid] > 0)
+    return lora_fail(LORA_EBUSY, "lora_adapter_unload: adapter " + std::to_string(aid) + " has " +
+                                     std::to_string(p->refs[aid]) + " active requests");
+  return drop_adapter(p, aid, stream, "lora_adapter_unload");
+}
+
+int lora_adapter_acquire(lora_pool* p, int32_t aid) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_acquire: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
+    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_acquire: adapter " + std::to_string(aid) + " is not loaded");
+  p->refs[aid] += 1;
+  return LORA_OK;
+}
+
+int lora_adapter_release(lora_pool* p, int32_t aid) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_release: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
+    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_release: adapter " + std::to_string(aid) + " is not loaded");
+  if (p->refs[aid] == 0)
+    return lora_fail(LORA_EINVAL, "lora_adapter_release: adapter " + std::to_string(aid) + " has no active request");
+  p->refs[aid] -= 1;
+  return LORA_OK;
+}
+
+int32_t lora_adapter_refs(const lora_pool* p, int32_t aid) {
+  if (!p || aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0) return -1;
+  return p->refs[aid];
+}
+
+int lora_pool_evict_idle(lora_pool* p, int64_t need, lora_stream_t stream, int32_t* evicted_host, int32_t* n_evicted) {
+  if (n_evicted) *n_evicted = 0;
+  if (!p || need < 0) return lora_fail(LORA_EINVAL, "lora_pool_evict_idle: bad arguments");
+  return evict_idle(p, need, stream, evicted_host, n_evicted, "lora_pool_evict_idle");
+}
+
+int lora_adapter_ensure(lora_pool* p, int32_t aid, int32_t rank, const void* const* A_host, const void* const* B_host,
+                        lora_stream_t stream, int32_t* table_out, int32_t* loaded_out, int32_t* evicted_host,
+                        int32_t* n_evicted) {
+  if (loaded_out) *loaded_out = 0;
+  if (n_evicted) *n_evicted = 0;
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_ensure: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters)
+    return lora_fail(LORA_EINVAL, "lora_adapter_ensure: adapter id " + std::to_string(aid) + " outside [0, max_adapters)");
+  if (p->rank[aid] != 0) {                       // resident: one more active request
+    if (rank != p->rank[aid])
+      return lora_fail(LORA_ERANK, "lora_adapter_ensure: adapter " + std::to_string(aid) + " is resident with rank " +
+                                       std::to_string(p->rank[aid]));
+    p->refs[aid] += 1;
+    if (table_out) std::memcpy(table_out, p->tables[aid].data(), p->tables[aid].size() * sizeof(int32_t));
+    return LORA_OK;
+  }
+  if (rank < 1 || rank > LORA_MAX_RANK)
+    return lora_fail(LORA_ERANK, "lora_adapter_ensure: rank " + std::to_string(rank) + " outside [1, 64]");
+  if (!p->planning && (!A_host || !B_host))
+    return lora_fail(LORA_EINVAL, "lora_adapter_ensure: A_host and B_host arrays are required");
+  if (!p->planning)                              // argument errors are found before anything is evicted
+    for (int s = 0; s < p->n_slots; ++s)
+      if (A_host[s] && !B_host[s]) return lora_fail(LORA_EINVAL, "lora_adapter_ensure: B_host[slot] is NULL where A_host[slot] is set");
+  int64_t n_present = 0;
+  for (int s = 0; s < p->n_slots; ++s) n_present += (A_host == nullptr || A_host[s] != nullptr);
+  const int64_t need = 2 * (int64_t)rank * n_present;
+  int rc = evict_idle(p, need, stream, evicted_host, n_evicted, "lora_adapter_ensure");
+  if (rc != LORA_OK) return rc;
+  rc = lora_adapter_load(p, aid, rank, A_host, B_host, stream, table_out);
+  if (rc != LORA_OK) return rc;
+  p->refs[aid] = 1;
+  if (loaded_out) *loaded_out = 1;
   return LORA_OK;
 }
 

@@ -51,6 +51,7 @@ typedef struct CUstream_st* lora_stream_t;  /* identical to cudaStream_t */
 #define LORA_EEXIST           -5   /* adapter id already loaded */
 #define LORA_ECUDA            -6   /* a CUDA runtime or driver call failed */
 #define LORA_EDEVICE          -7   /* a device-side check failed (see lora_status) */
+#define LORA_EBUSY            -8   /* the adapter has active requests */
 
 #define LORA_MAX_RANK      64
 #define LORA_MAX_ADAPTERS  16384    /* adapter ids are indices in [0, max_adapters) */
@@ -149,9 +150,10 @@ int lora_adapter_load(lora_pool* pool, int32_t adapter_id, int32_t rank,
                       const void* const* A_host, const void* const* B_host,
                       lora_stream_t stream, int32_t* page_table_host);
 
-/* Return an adapter's pages to the free list and clear its device page table (enqueued on
- * `stream`; work already enqueued before it on that stream still sees the adapter).
- * LORA_EUNKNOWN_ADAPTER if it is not loaded. */
+/* Return an adapter's pages to the free list (in the order they were taken) and clear its
+ * device page table (enqueued on `stream`; work already enqueued before it on that stream
+ * still sees the adapter).  LORA_EUNKNOWN_ADAPTER if it is not loaded, LORA_EBUSY if it has
+ * active requests (see lora_adapter_acquire). */
 int lora_adapter_unload(lora_pool* pool, int32_t adapter_id, lora_stream_t stream);
 
 /* Device workspace bytes lora_segments_init needs for batches of up to T_max tokens
@@ -216,6 +218,48 @@ int lora_linear_forward(lora_pool* pool, const lora_segments* seg, int32_t slot,
 int lora_linear_forward_group(lora_pool* pool, const lora_segments* seg, int32_t n, const int32_t* slots_host,
                               const void* x, const void* const* W_host, void* const* y_host,
                               float* const* delta_dbg_host, lora_stream_t stream);
+
+/*
+ * Adapter lifecycle in the unified pool ("S-LoRA, in depth", "Unified paging": the pool sketch
+ * counts each resident adapter's active requests; ensure_adapter loads an adapter that is not
+ * resident, first evicting idle adapters, those with no active request, to free pages; "The
+ * architecture": when an adapter has no active requests left, its pages can be reclaimed for
+ * KV cache or for another adapter).
+ *   lora_adapter_load leaves a new adapter resident and idle (0 active requests);
+ *   lora_adapter_acquire / lora_adapter_release add / remove one active request
+ *     (LORA_EUNKNOWN_ADAPTER if not resident; release of an idle adapter is LORA_EINVAL);
+ *   lora_adapter_refs returns the count, or -1 if the adapter is not resident;
+ *   lora_adapter_unload refuses an adapter with active requests (LORA_EBUSY).
+ */
+int lora_adapter_acquire(lora_pool* pool, int32_t adapter_id);
+int lora_adapter_release(lora_pool* pool, int32_t adapter_id);
+int32_t lora_adapter_refs(const lora_pool* pool, int32_t adapter_id);
+
+/*
+ * Evict idle adapters, the one loaded earliest first, until at least `need` pages are free
+ * (the sketch's evict_idle_adapters), clearing their device page tables in `stream` order as
+ * lora_adapter_unload does: work enqueued on `stream` before the call still sees them.
+ *   evicted_host  nullable host int32 [max_adapters]: receives the evicted ids in order;
+ *   n_evicted     nullable: receives their count.
+ * If evicting every idle adapter would still leave fewer than `need` pages free, nothing is
+ * evicted and the call returns LORA_ENOPAGES (the sketch evicts them and still fails).
+ */
+int lora_pool_evict_idle(lora_pool* pool, int64_t need, lora_stream_t stream, int32_t* evicted_host,
+                         int32_t* n_evicted);
+
+/*
+ * The sketch's ensure_adapter.  If `adapter_id` is resident it gets one more active request
+ * (A_host and B_host are not read; `rank` must equal the resident rank, else LORA_ERANK) and
+ * *loaded_out = 0.  Otherwise idle adapters are evicted as lora_pool_evict_idle does to make
+ * room for its pages, the adapter is loaded as lora_adapter_load does (same arguments, same
+ * page order) and given one active request, and *loaded_out = 1.  table_out as for
+ * lora_adapter_load; evicted_host / n_evicted as for lora_pool_evict_idle (all nullable).
+ * LORA_ENOPAGES (nothing evicted, nothing loaded) if even evicting every idle adapter would
+ * not free enough pages.
+ */
+int lora_adapter_ensure(lora_pool* pool, int32_t adapter_id, int32_t rank, const void* const* A_host,
+                        const void* const* B_host, lora_stream_t stream, int32_t* table_out,
+                        int32_t* loaded_out, int32_t* evicted_host, int32_t* n_evicted);
 
 /* Synchronise `stream`, read and clear the device error word.  LORA_OK, or LORA_EDEVICE
  * with lora_last_error() naming the failed check (unknown adapter id, page id out of

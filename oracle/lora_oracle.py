@@ -48,6 +48,7 @@ ENOPAGES = -2
 EUNKNOWN_ADAPTER = -3
 ERANK = -4
 EEXIST = -5
+EBUSY = -8
 
 MAX_RANK = 64
 
@@ -66,10 +67,16 @@ class PoolModel:
 
     Follows the sketch's semantics: ``free`` is a list of page ids and pages
     are taken with ``pop()`` from its end; pages given back are appended.
+    Adapters carry the sketch's count of active requests: ``ensure`` gives a
+    resident adapter one more, or loads a new one with one (making room by
+    evicting idle adapters, those with no active request, in the order they
+    were loaded); ``evict_idle`` is the sketch's eviction on its own.
     Differences from the sketch, each a fix rather than a new rule:
-      * a failed request (too few free pages) changes nothing;
-      * there is no reference count: unload is explicit (the sketch never
-        decrements its count, so its idle-adapter eviction could never fire);
+      * a failed request (too few free pages) changes nothing, and an eviction
+        that could not free enough pages evicts nothing;
+      * requests end with an explicit ``release`` (the sketch never decrements
+        its count, so its idle-adapter eviction could never fire); ``load``
+        makes a resident, idle adapter and ``unload`` refuses a busy one;
       * KV/filler pages are reserved and released by explicit page lists
         (the sketch's ``grow_kv`` per request).
     Page tables: for an adapter of rank r over ``n_slots`` projection slots,
@@ -87,6 +94,7 @@ class PoolModel:
         self.reserved: set = set()
         self.tables: Dict[int, np.ndarray] = {}
         self.ranks: Dict[int, int] = {}
+        self.refs: Dict[int, int] = {}          # active requests per resident adapter, in load order
 
     @staticmethod
     def pages_for_adapter(rank: int, layers: int, projections: int) -> int:
@@ -130,15 +138,78 @@ class PoolModel:
                     table[s, half, j] = self.free.pop()
         self.tables[adapter] = table
         self.ranks[adapter] = rank
+        self.refs[adapter] = 0
         return OK, table
 
     def unload(self, adapter: int) -> int:
         if adapter not in self.tables:
             return EUNKNOWN_ADAPTER
+        if self.refs[adapter] > 0:
+            return EBUSY
+        self._drop(adapter)
+        return OK
+
+    def _drop(self, adapter: int) -> None:
         table = self.tables.pop(adapter)
         self.ranks.pop(adapter)
+        self.refs.pop(adapter)
         self.free.extend(int(p) for p in table.reshape(-1) if p >= 0)
+
+    # ---- adapter lifecycle: the sketch's adapter_refs, ensure_adapter, evict_idle_adapters ----
+    def acquire(self, adapter: int) -> int:
+        if adapter not in self.tables:
+            return EUNKNOWN_ADAPTER
+        self.refs[adapter] += 1
         return OK
+
+    def release_adapter(self, adapter: int) -> int:
+        if adapter not in self.tables:
+            return EUNKNOWN_ADAPTER
+        if self.refs[adapter] == 0:
+            return EINVAL
+        self.refs[adapter] -= 1
+        return OK
+
+    def evict_idle(self, need: int):
+        """Evict idle adapters, oldest load first, until at least ``need`` pages are free.
+        Returns (status, evicted ids).  If evicting every idle adapter would still leave fewer
+        than ``need`` pages free, nothing is evicted (ENOPAGES)."""
+        if need < 0:
+            return EINVAL, []
+        idle = [a for a, n in self.refs.items() if n == 0]
+        freeable = sum(int((self.tables[a] >= 0).sum()) for a in idle)
+        if len(self.free) + freeable < need:
+            return ENOPAGES, []
+        evicted = []
+        for a in idle:
+            if len(self.free) >= need:
+                break
+            self._drop(a)
+            evicted.append(a)
+        return OK, evicted
+
+    def ensure(self, adapter: int, rank: int, present: Sequence[bool]):
+        """The sketch's ensure_adapter.  Returns (status, table, loaded, evicted): a resident
+        adapter gets one more active request (its factors are not looked at; a different rank
+        is ERANK: the rank is part of the adapter); otherwise idle adapters are evicted to make
+        room and the adapter is loaded with one request."""
+        if adapter in self.tables:
+            if rank != self.ranks[adapter]:
+                return ERANK, None, False, []
+            self.refs[adapter] += 1
+            return OK, self.tables[adapter], False, []
+        if not (0 <= adapter < self.max_adapters) or len(present) != self.n_slots:
+            return EINVAL, None, False, []
+        if not (1 <= rank <= MAX_RANK):
+            return ERANK, None, False, []
+        need = 2 * rank * sum(1 for p in present if p)
+        st, evicted = self.evict_idle(need)
+        if st != OK:
+            return st, None, False, []
+        st, table = self.load(adapter, rank, present)
+        assert st == OK
+        self.refs[adapter] = 1
+        return OK, table, True, evicted
 
     def stats(self) -> dict:
         adapter_pages = sum(int((t >= 0).sum()) for t in self.tables.values())

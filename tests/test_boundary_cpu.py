@@ -1,5 +1,6 @@
 """The C boundary without a GPU: the library loads, exports every declared entry point, and
 its host page bookkeeping (planning pools) matches the oracle's pool model exactly."""
+import json
 import os
 import re
 import subprocess
@@ -213,3 +214,63 @@ def test_group_workspace_sizes_and_argument_checks(L):
         L.lora_linear_forward_group(pool, seg, [0, 1], 16, [16, 16], [32, 48], stream=0)
     assert e.value.code == L.LORA_EINVAL
     L.lora_pool_destroy(pool)
+
+
+def test_pool_lifecycle_golden_scenario_library(L):
+    """The C pool's adapter lifecycle on the hand-worked scenario of the pool sketch."""
+    from pool_scenario import LibraryDriver, run_golden
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "pool_lifecycle_scenario.json")))
+    d = LibraryDriver(L, g["pool"]["num_pages"], g["pool"]["n_slots"], g["pool"]["max_adapters"])
+    try:
+        assert run_golden(d, g["steps"]) == []
+    finally:
+        d.close()
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_pool_lifecycle_matches_oracle(L, seed):
+    """Random ensure / acquire / release / reserve / unload / evict sequences: statuses, page
+    tables, evicted ids, active-request counts and page accounting bit-exact with the oracle."""
+    from pool_scenario import LibraryDriver, OracleDriver, apply_op, random_ops
+    n_pages, n_slots, n_ad = 120, 2, 12
+    order = np.random.default_rng(100 + seed).permutation(n_pages)
+    lib = LibraryDriver(L, n_pages, n_slots, n_ad, page_order=order)
+    ora = OracleDriver(n_pages, n_slots, n_ad, page_order=order)
+    try:
+        res_l, res_o = [], []
+        for i, op in enumerate(random_ops(seed, 400, n_ad)):
+            a, b = apply_op(lib, op, res_l), apply_op(ora, op, res_o)
+            assert a == b, f"op {i} {op}: library {a} vs oracle {b}"
+            assert lib.stats() == ora.stats(), f"op {i} {op}"
+            assert [lib.refs(k) for k in range(n_ad)] == [ora.refs(k) for k in range(n_ad)], f"op {i} {op}"
+    finally:
+        lib.close()
+
+
+def test_pool_lifecycle_errors(L):
+    pool = L.lora_pool_create(None, 64, 64, 1, 4)
+    try:
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_acquire(pool, 1)
+        assert e.value.code == L.LORA_EUNKNOWN_ADAPTER
+        L.lora_adapter_load(pool, 1, 4, None, None, 1, planning=True)
+        assert L.lora_adapter_refs(pool, 1) == 0 and L.lora_adapter_refs(pool, 2) == -1
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_release(pool, 1)                  # idle: nothing to release
+        assert e.value.code == L.LORA_EINVAL
+        tab, loaded, ev = L.lora_adapter_ensure(pool, 1, 4, None, None, 1, 4, planning=True)
+        assert not loaded and ev == [] and L.lora_adapter_refs(pool, 1) == 1
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_ensure(pool, 1, 8, None, None, 1, 4, planning=True)   # resident with rank 4
+        assert e.value.code == L.LORA_ERANK
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_unload(pool, 1, planning=True)
+        assert e.value.code == L.LORA_EBUSY
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_evict_idle(pool, 100, 4, planning=True)
+        assert e.value.code == L.LORA_ENOPAGES
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_ensure(pool, 4, 4, None, None, 1, 4, planning=True)    # id out of range
+        assert e.value.code == L.LORA_EINVAL
+    finally:
+        L.lora_pool_destroy(pool)

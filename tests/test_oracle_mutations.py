@@ -109,3 +109,59 @@ def test_front_pop_changes_tables_but_not_outputs():
     a = L.PoolModel(20, 1, 2, page_order=np.arange(20))
     b = _PoolFrontPop(20, 1, 2, page_order=np.arange(20))
     assert not np.array_equal(a.load(0, 3, [True])[1], b.load(0, 3, [True])[1])
+
+
+# ---- pool lifecycle: plausible mistakes in the sketch's bookkeeping, caught by the hand-worked
+# scenario of tests/golden/pool_lifecycle_scenario.json
+class _NewestFirst(O.PoolModel):
+    def evict_idle(self, need):
+        saved = self.refs
+        self.refs = dict(reversed(list(saved.items())))
+        try:
+            return super().evict_idle(need)
+        finally:
+            self.refs = {a: n for a, n in saved.items() if a in self.tables}
+
+
+class _EvictsBusy(O.PoolModel):
+    def evict_idle(self, need):
+        saved = dict(self.refs)
+        self.refs = {a: 0 for a in self.refs}
+        st, ev = super().evict_idle(need)
+        self.refs = {a: n for a, n in saved.items() if a in self.tables}
+        return st, ev
+
+
+class _EvictsThenFails(O.PoolModel):          # the sketch taken literally: evictions stand on failure
+    def evict_idle(self, need):
+        for a in [a for a, n in self.refs.items() if n == 0]:
+            if len(self.free) >= need:
+                break
+            self._drop(a)
+        return (O.OK if len(self.free) >= need else O.ENOPAGES), []
+
+
+class _PagesBackReversed(O.PoolModel):
+    def _drop(self, adapter):
+        table = self.tables.pop(adapter)
+        self.ranks.pop(adapter)
+        self.refs.pop(adapter)
+        self.free.extend(int(p) for p in table.reshape(-1)[::-1] if p >= 0)
+
+
+class _ResidentNotCounted(O.PoolModel):
+    def ensure(self, adapter, rank, present):
+        if adapter in self.tables:
+            return O.OK, self.tables[adapter], False, []
+        return super().ensure(adapter, rank, present)
+
+
+@pytest.mark.parametrize("cls", [_NewestFirst, _EvictsBusy, _EvictsThenFails, _PagesBackReversed, _ResidentNotCounted],
+                         ids=lambda c: c.__name__)
+def test_lifecycle_mutation_is_caught(cls):
+    import json
+    import os
+    from pool_scenario import OracleDriver, run_golden
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pool_lifecycle_scenario.json")))
+    d = OracleDriver(g["pool"]["num_pages"], g["pool"]["n_slots"], g["pool"]["max_adapters"], model_cls=cls)
+    assert run_golden(d, g["steps"]) != [], f"{cls.__name__} passes the scenario"

@@ -100,3 +100,39 @@ def test_bf16_round_ties_to_even():
     vals = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, 256.0, -3.5])
     got = O.bf16_round(vals)
     assert got.tolist() == [1.0, 1.0, 1.0 + 2**-6, 256.0, -3.5]
+
+
+def test_pool_lifecycle_golden_scenario():
+    """The pool sketch's adapter lifecycle ("Unified paging"), worked out by hand on 40 pages:
+    page ids taken, active-request counts, eviction order and failures."""
+    from pool_scenario import OracleDriver, run_golden
+    g = json.load(open(os.path.join(GOLDEN, "pool_lifecycle_scenario.json")))
+    d = OracleDriver(g["pool"]["num_pages"], g["pool"]["n_slots"], g["pool"]["max_adapters"])
+    assert run_golden(d, g["steps"]) == []
+
+
+def test_pool_lifecycle_invariants():
+    """Random lifecycle sequences: every page is in exactly one place, only idle adapters are
+    evicted, a successful ensure leaves the adapter resident with an active request, and a
+    failed ensure or eviction changes nothing."""
+    from pool_scenario import OracleDriver, apply_op, random_ops
+    n_pages, n_ad = 96, 10
+    for seed in range(20):
+        d = OracleDriver(n_pages, 2, n_ad, page_order=np.random.default_rng(seed).permutation(n_pages))
+        reserved = []
+        for op in random_ops(seed, 300, n_ad):
+            refs_before = dict(d.m.refs)
+            free_before = list(d.m.free)
+            rec = apply_op(d, op, reserved)
+            pages = [int(p) for t in d.m.tables.values() for p in t.reshape(-1) if p >= 0]
+            assert len(pages) == len(set(pages))
+            assert not set(pages) & set(d.m.free) and not set(pages) & d.m.reserved
+            assert not set(d.m.free) & d.m.reserved
+            assert len(pages) + len(d.m.free) + len(d.m.reserved) == n_pages
+            if rec[0] in ("ensure", "evict_idle"):
+                for a in rec[-1]:
+                    assert refs_before.get(a) == 0, f"busy adapter {a} evicted"
+                if rec[1] == O.ENOPAGES:
+                    assert d.m.refs == refs_before and d.m.free == free_before
+            if rec[0] == "ensure" and rec[1] == O.OK:
+                assert d.m.refs[op[1]] >= 1
