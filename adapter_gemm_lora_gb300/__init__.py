@@ -30,6 +30,9 @@ LORA_EEXIST = -5
 LORA_ECUDA = -6
 LORA_EDEVICE = -7
 LORA_EBUSY = -8
+LORA_EVICT_LOAD_ORDER = 0
+LORA_EVICT_LRU = 1
+LORA_EVICT_FARTHEST = 2
 LORA_MAX_RANK = 64
 LORA_MAX_ADAPTERS = 16384
 LORA_MAX_TOKENS = 65536
@@ -43,7 +46,7 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc",
             "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group",
             "lora_adapter_acquire", "lora_adapter_release", "lora_adapter_refs", "lora_pool_evict_idle",
-            "lora_adapter_ensure"]
+            "lora_adapter_ensure", "lora_pool_set_eviction"]
 KINDS = ("segments", "delta", "gemm", "scatter")
 
 
@@ -105,6 +108,7 @@ def _load():
         "lora_adapter_refs": (I32, [VP, I32]),
         "lora_pool_evict_idle": (I32, [VP, I64, VP, VP, VP]),
         "lora_adapter_ensure": (I32, [VP, I32, I32, VP, VP, VP, VP, VP, VP, VP]),
+        "lora_pool_set_eviction": (I32, [VP, I32, VP, I64, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -208,6 +212,12 @@ def lora_adapter_acquire(pool, adapter_id: int) -> None:
 
 def lora_adapter_release(pool, adapter_id: int) -> None:
     _check(_load().lora_adapter_release(pool, adapter_id))
+
+
+def lora_pool_set_eviction(pool, policy: int, future=None, lookahead: int = 0) -> None:
+    """Eviction rule for idle adapters; `future` = upcoming adapter requests (farthest-future rule)."""
+    fut = np.ascontiguousarray(np.zeros(0) if future is None else future, dtype=np.int32)
+    _check(_load().lora_pool_set_eviction(pool, policy, _ptr(fut) if fut.size else None, fut.size, lookahead))
 
 
 def lora_adapter_refs(pool, adapter_id: int) -> int:

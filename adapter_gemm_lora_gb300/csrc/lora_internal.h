@@ -36,8 +36,13 @@ struct lora_pool {
   std::vector<int32_t> rank;                      // per adapter id; 0 = not loaded
   std::vector<std::vector<int32_t>> tables;       // per adapter id: [n_slots][2][rank]
   std::vector<int32_t> refs;                      // per adapter id: active requests
-  std::vector<int64_t> load_seq;                  // per adapter id: order of its load (eviction order)
+  std::vector<int64_t> load_seq;                  // per adapter id: order of its load
   int64_t next_seq = 0;
+  std::vector<int64_t> last_use;                  // per adapter id: clock of its last load / ensure / acquire
+  int64_t use_clock = 0;
+  int32_t evict_policy = LORA_EVICT_LOAD_ORDER;   // which idle adapter goes first
+  std::vector<int32_t> future;                    // upcoming adapter requests (farthest-future rule)
+  int32_t lookahead = 0;                          // entries of `future` looked at; <= 0: all
   int64_t adapter_pages = 0;
   int64_t reserved_pages = 0;
   int32_t resident = 0;

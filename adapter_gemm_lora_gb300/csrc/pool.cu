@@ -188,6 +188,7 @@ int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slo
   p->tables.resize(max_adapters);
   p->refs.assign(max_adapters, 0);
   p->load_seq.assign(max_adapters, 0);
+  p->last_use.assign(max_adapters, 0);
 
   if (!p->planning) {
     cudaError_t e = cudaGetDevice(&p->device);
@@ -351,6 +352,7 @@ int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const
   p->rank[aid] = rank;
   p->refs[aid] = 0;
   p->load_seq[aid] = p->next_seq++;
+  p->last_use[aid] = ++p->use_clock;
   p->tables[aid] = table;
   p->adapter_pages += need;
   p->resident += 1;
@@ -392,13 +394,30 @@ int64_t adapter_page_count(const lora_pool* p, int32_t aid) {
   return n;
 }
 
-// Idle resident adapters in eviction order (earliest load first) and how many of them must go
-// for `need` pages to be free; -1 if all of them would not be enough.
+// Idle resident adapters in eviction order (the pool's rule) and how many of them must go for
+// `need` pages to be free; -1 if all of them would not be enough.
 int evict_plan(const lora_pool* p, int64_t need, std::vector<int32_t>& order) {
   order.clear();
   for (int32_t a = 0; a < p->max_adapters; ++a)
     if (p->rank[a] != 0 && p->refs[a] == 0) order.push_back(a);
-  std::sort(order.begin(), order.end(), [p](int32_t a, int32_t b) { return p->load_seq[a] < p->load_seq[b]; });
+  if (p->evict_policy == LORA_EVICT_LRU) {
+    std::sort(order.begin(), order.end(), [p](int32_t a, int32_t b) { return p->last_use[a] < p->last_use[b]; });
+  } else if (p->evict_policy == LORA_EVICT_FARTHEST) {
+    // next request of each idle adapter within the horizon; INT64_MAX = not requested there
+    const int64_t horizon = p->lookahead > 0 ? std::min<int64_t>(p->lookahead, (int64_t)p->future.size())
+                                             : (int64_t)p->future.size();
+    std::vector<int64_t> nxt(p->max_adapters, INT64_MAX);
+    for (int64_t i = horizon - 1; i >= 0; --i) {
+      const int32_t a = p->future[i];
+      if (a >= 0 && a < p->max_adapters) nxt[a] = i;
+    }
+    std::sort(order.begin(), order.end(), [p, &nxt](int32_t a, int32_t b) {
+      if (nxt[a] != nxt[b]) return nxt[a] > nxt[b];    // farthest next request first
+      return p->last_use[a] < p->last_use[b];          // not requested in the horizon: LRU
+    });
+  } else {
+    std::sort(order.begin(), order.end(), [p](int32_t a, int32_t b) { return p->load_seq[a] < p->load_seq[b]; });
+  }
   int64_t free_pages = (int64_t)p->free_list.size();
   int k = 0;
   while (free_pages < need && k < (int)order.size()) free_pages += adapter_page_count(p, order[k++]);
@@ -440,6 +459,17 @@ int lora_adapter_acquire(lora_pool* p, int32_t aid) {
   if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
     return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_acquire: adapter " + std::to_string(aid) + " is not loaded");
   p->refs[aid] += 1;
+  p->last_use[aid] = ++p->use_clock;
+  return LORA_OK;
+}
+
+int lora_pool_set_eviction(lora_pool* p, int32_t policy, const int32_t* future, int64_t n_future, int32_t lookahead) {
+  if (!p || n_future < 0 || (n_future > 0 && !future) ||
+      (policy != LORA_EVICT_LOAD_ORDER && policy != LORA_EVICT_LRU && policy != LORA_EVICT_FARTHEST))
+    return lora_fail(LORA_EINVAL, "lora_pool_set_eviction: bad arguments");
+  p->evict_policy = policy;
+  p->future.assign(future, future + n_future);
+  p->lookahead = lookahead;
   return LORA_OK;
 }
 
@@ -477,6 +507,7 @@ int lora_adapter_ensure(lora_pool* p, int32_t aid, int32_t rank, const void* con
       return lora_fail(LORA_ERANK, "lora_adapter_ensure: adapter " + std::to_string(aid) + " is resident with rank " +
                                        std::to_string(p->rank[aid]));
     p->refs[aid] += 1;
+    p->last_use[aid] = ++p->use_clock;
     if (table_out) std::memcpy(table_out, p->tables[aid].data(), p->tables[aid].size() * sizeof(int32_t));
     return LORA_OK;
   }

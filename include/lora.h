@@ -236,8 +236,28 @@ int lora_adapter_release(lora_pool* pool, int32_t adapter_id);
 int32_t lora_adapter_refs(const lora_pool* pool, int32_t adapter_id);
 
 /*
- * Evict idle adapters, the one loaded earliest first, until at least `need` pages are free
- * (the sketch's evict_idle_adapters), clearing their device page tables in `stream` order as
+ * Which idle adapter is evicted first ("Fewer Expert Transfers Without Changing Routing",
+ * sections "A better eviction rule cuts transfers without changing routing" and "Limited
+ * foresight": an eviction choice changes only future loads, never the current batch's work):
+ *   LORA_EVICT_LOAD_ORDER  the one loaded earliest (the pool sketch; the default);
+ *   LORA_EVICT_LRU         the least recently used (last load, ensure or acquire);
+ *   LORA_EVICT_FARTHEST    the one whose next request in `future_host` lies farthest; only the
+ *                          first `lookahead` entries are looked at (<= 0: all of them), and the
+ *                          adapters not requested there count as equal and go first, least
+ *                          recently used first.
+ * future_host (nullable when n_future is 0) is copied; callers refresh it as their queue moves.
+ * LORA_EINVAL for an unknown policy or n_future < 0.
+ */
+#define LORA_EVICT_LOAD_ORDER 0
+#define LORA_EVICT_LRU        1
+#define LORA_EVICT_FARTHEST   2
+int lora_pool_set_eviction(lora_pool* pool, int32_t policy, const int32_t* future_host, int64_t n_future,
+                           int32_t lookahead);
+
+/*
+ * Evict idle adapters, in the order of the pool's eviction rule (lora_pool_set_eviction; by
+ * default the one loaded earliest first), until at least `need` pages are free (the sketch's
+ * evict_idle_adapters), clearing their device page tables in `stream` order as
  * lora_adapter_unload does: work enqueued on `stream` before the call still sees them.
  *   evicted_host  nullable host int32 [max_adapters]: receives the evicted ids in order;
  *   n_evicted     nullable: receives their count.

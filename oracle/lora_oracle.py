@@ -52,6 +52,11 @@ EBUSY = -8
 
 MAX_RANK = 64
 
+# Eviction rules for idle adapters.
+EVICT_LOAD_ORDER = 0      # the pool sketch: the adapter loaded earliest
+EVICT_LRU = 1             # least recently used (loaded, ensured or acquired)
+EVICT_FARTHEST = 2        # next use farthest in the known future; beyond the lookahead, LRU
+
 
 def bf16_to_f64(bits) -> np.ndarray:
     """Decode bf16 bit patterns (uint16) to fp64 exactly."""
@@ -95,6 +100,13 @@ class PoolModel:
         self.tables: Dict[int, np.ndarray] = {}
         self.ranks: Dict[int, int] = {}
         self.refs: Dict[int, int] = {}          # active requests per resident adapter, in load order
+        # eviction rule ("Fewer Expert Transfers...", section "A better eviction rule cuts transfers
+        # without changing routing" and appendix "Limited foresight"): which idle adapter goes first
+        self.policy = EVICT_LOAD_ORDER
+        self.future: List[int] = []             # upcoming adapter requests, in order
+        self.lookahead = 0                      # requests of `future` looked at (<= 0: all)
+        self.clock = 0
+        self.last_use: Dict[int, int] = {}
 
     @staticmethod
     def pages_for_adapter(rank: int, layers: int, projections: int) -> int:
@@ -139,6 +151,7 @@ class PoolModel:
         self.tables[adapter] = table
         self.ranks[adapter] = rank
         self.refs[adapter] = 0
+        self._touch(adapter)
         return OK, table
 
     def unload(self, adapter: int) -> int:
@@ -153,6 +166,7 @@ class PoolModel:
         table = self.tables.pop(adapter)
         self.ranks.pop(adapter)
         self.refs.pop(adapter)
+        self.last_use.pop(adapter, None)
         self.free.extend(int(p) for p in table.reshape(-1) if p >= 0)
 
     # ---- adapter lifecycle: the sketch's adapter_refs, ensure_adapter, evict_idle_adapters ----
@@ -160,7 +174,37 @@ class PoolModel:
         if adapter not in self.tables:
             return EUNKNOWN_ADAPTER
         self.refs[adapter] += 1
+        self._touch(adapter)
         return OK
+
+    def _touch(self, adapter: int) -> None:
+        self.clock += 1
+        self.last_use[adapter] = self.clock
+
+    def set_eviction(self, policy: int, future: Sequence[int] = (), lookahead: int = 0) -> int:
+        if policy not in (EVICT_LOAD_ORDER, EVICT_LRU, EVICT_FARTHEST):
+            return EINVAL
+        self.policy = policy
+        self.future = [int(a) for a in future]
+        self.lookahead = int(lookahead)
+        return OK
+
+    def eviction_order(self) -> List[int]:
+        """Idle resident adapters, the first to evict first."""
+        idle = [a for a, n in self.refs.items() if n == 0]          # load order
+        if self.policy == EVICT_LRU:
+            return sorted(idle, key=lambda a: self.last_use[a])
+        if self.policy == EVICT_FARTHEST:
+            horizon = self.future if self.lookahead <= 0 else self.future[:self.lookahead]
+            nxt = {}
+            for i, a in enumerate(horizon):
+                nxt.setdefault(a, i)
+            beyond = [a for a in idle if a not in nxt]
+            seen = [a for a in idle if a in nxt]
+            # never used within the horizon: all equal, least recently used first; then the
+            # rest, next use farthest first
+            return sorted(beyond, key=lambda a: self.last_use[a]) + sorted(seen, key=lambda a: -nxt[a])
+        return idle
 
     def release_adapter(self, adapter: int) -> int:
         if adapter not in self.tables:
@@ -176,7 +220,7 @@ class PoolModel:
         than ``need`` pages free, nothing is evicted (ENOPAGES)."""
         if need < 0:
             return EINVAL, []
-        idle = [a for a, n in self.refs.items() if n == 0]
+        idle = self.eviction_order()
         freeable = sum(int((self.tables[a] >= 0).sum()) for a in idle)
         if len(self.free) + freeable < need:
             return ENOPAGES, []
@@ -197,6 +241,7 @@ class PoolModel:
             if rank != self.ranks[adapter]:
                 return ERANK, None, False, []
             self.refs[adapter] += 1
+            self._touch(adapter)
             return OK, self.tables[adapter], False, []
         if not (0 <= adapter < self.max_adapters) or len(present) != self.n_slots:
             return EINVAL, None, False, []

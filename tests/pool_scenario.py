@@ -36,6 +36,9 @@ class OracleDriver:
     def evict_idle(self, need):
         return self.m.evict_idle(need)
 
+    def set_eviction(self, policy, future=(), lookahead=0):
+        return self.m.set_eviction(policy, future, lookahead)
+
     def refs(self, a):
         return self.m.refs.get(a, -1)
 
@@ -88,6 +91,9 @@ class LibraryDriver:
     def evict_idle(self, need):
         st, ev = self._call(self.L.lora_pool_evict_idle, self.p, need, self.max_adapters, None, True)
         return st, ([] if ev is None else ev)
+
+    def set_eviction(self, policy, future=(), lookahead=0):
+        return self._call(self.L.lora_pool_set_eviction, self.p, policy, list(future), lookahead)[0]
 
     def refs(self, a):
         return self.L.lora_adapter_refs(self.p, a)
@@ -172,10 +178,13 @@ def random_ops(seed, n_ops, max_adapters):
             ops.append(("reserve", int(rng.integers(0, 12))))
         elif k < 82:
             ops.append(("release_reserved",))
-        elif k < 90:
+        elif k < 88:
             ops.append(("unload", a))
-        else:
+        elif k < 96:
             ops.append(("evict_idle", int(rng.integers(0, 80))))
+        else:
+            fut = rng.integers(0, max_adapters, size=int(rng.integers(0, 20))).tolist()
+            ops.append(("set_eviction", int(rng.integers(0, 3)), fut, int(rng.integers(-1, 8))))
     return ops
 
 
@@ -203,6 +212,8 @@ def apply_op(driver, op, reserved_lists):
     if kind == "evict_idle":
         st, ev = driver.evict_idle(op[1])
         return ("evict_idle", st, tuple(ev))
+    if kind == "set_eviction":
+        return ("set_eviction", driver.set_eviction(op[1], op[2], op[3]))
     raise ValueError(kind)
 
 
@@ -210,3 +221,37 @@ def _freeze(v):
     if isinstance(v, list):
         return tuple(_freeze(x) for x in v)
     return v
+
+
+def cache_loads(driver_factory, stream, capacity, policy, lookahead=0, foresight=True):
+    """Serve a request stream one request at a time through a pool that holds `capacity`
+    adapters of rank 1 (one slot): ensure the adapter, then end its request.  Returns the number
+    of loads.  With the farthest-future rule the pool is told the requests after the current one
+    (none when `foresight` is False)."""
+    d = driver_factory(capacity * 2)
+    loads = 0
+    for i, a in enumerate(stream):
+        d.set_eviction(policy, list(stream[i + 1:]) if foresight else [], lookahead)
+        st, tab, loaded, ev = d.ensure(int(a), 1)
+        assert st == 0, (i, a, st)
+        loads += int(loaded)
+        assert d.release_adapter(int(a)) == 0
+    return loads
+
+
+def min_loads(stream, capacity):
+    """Fewest loads any eviction choice can give (exhaustive search over cache contents)."""
+    from functools import lru_cache
+    stream = tuple(int(a) for a in stream)
+
+    @lru_cache(maxsize=None)
+    def best(i, cache):
+        if i == len(stream):
+            return 0
+        a = stream[i]
+        if a in cache:
+            return best(i + 1, cache)
+        if len(cache) < capacity:
+            return 1 + best(i + 1, tuple(sorted(cache + (a,))))
+        return 1 + min(best(i + 1, tuple(sorted([c for c in cache if c != v] + [a]))) for v in cache)
+    return best(0, ())

@@ -274,3 +274,46 @@ def test_pool_lifecycle_errors(L):
         assert e.value.code == L.LORA_EINVAL
     finally:
         L.lora_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("policy", [0, 1, 2])
+def test_eviction_rules_match_oracle_on_request_streams(L, policy):
+    """Seeded Zipf request streams served one at a time through a pool of 24 adapters' pages:
+    the C pool loads exactly the adapters the oracle loads, under each eviction rule."""
+    from pool_scenario import LibraryDriver, OracleDriver
+    rng = np.random.default_rng(30 + policy)
+    n_ad, cap = 60, 24
+    p = 1.0 / np.arange(1, n_ad + 1) ** 0.8
+    stream = rng.choice(n_ad, size=400, p=p / p.sum()).tolist()
+    lib = LibraryDriver(L, cap * 2, 1, n_ad)
+    ora = OracleDriver(cap * 2, 1, n_ad)
+    try:
+        for i, a in enumerate(stream):
+            fut = stream[i + 1:]
+            for d in (lib, ora):
+                assert d.set_eviction(policy, fut, 16 if policy == 2 else 0) == 0
+            got, want = lib.ensure(a, 1), ora.ensure(a, 1)
+            assert got[0] == 0 and got == want, f"request {i} ({a}): {got} vs {want}"
+            assert lib.release_adapter(a) == ora.release_adapter(a) == 0
+    finally:
+        lib.close()
+
+
+def test_set_eviction_rejects_bad_arguments(L):
+    pool = L.lora_pool_create(None, 8, 64, 1, 2)
+    try:
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_set_eviction(pool, 3)
+        assert e.value.code == L.LORA_EINVAL
+    finally:
+        L.lora_pool_destroy(pool)
+
+
+def test_eviction_sim_tool_runs(L):
+    """The capacity-planning simulation runs on the library's planning pools and reports loads
+    between the number of distinct adapters requested and the number of requests."""
+    from adapter_gemm_lora_gb300 import eviction_sim
+    out = eviction_sim.main(["--adapters", "40", "--requests", "300", "--slots", "4", "--lookaheads", "2,0"])
+    assert set(out["policies"]) == {"load_order", "lru", "farthest_k2", "farthest_full_window"}
+    for rec in out["policies"].values():
+        assert 0 < rec["loads_per_request"] <= 1

@@ -165,3 +165,42 @@ def test_lifecycle_mutation_is_caught(cls):
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pool_lifecycle_scenario.json")))
     d = OracleDriver(g["pool"]["num_pages"], g["pool"]["n_slots"], g["pool"]["max_adapters"], model_cls=cls)
     assert run_golden(d, g["steps"]) != [], f"{cls.__name__} passes the scenario"
+
+
+# ---- eviction rules: plausible mistakes, caught by the eviction pins (toy sequences, Belady's
+# optimum by exhaustive search, the rule without foresight reducing to LRU)
+class _NearestFutureFirst(O.PoolModel):
+    def eviction_order(self):
+        if self.policy != O.EVICT_FARTHEST:
+            return super().eviction_order()
+        return list(reversed(super().eviction_order()))
+
+
+class _UnrequestedLast(O.PoolModel):
+    def eviction_order(self):
+        order = super().eviction_order()
+        if self.policy != O.EVICT_FARTHEST:
+            return order
+        horizon = self.future if self.lookahead <= 0 else self.future[:self.lookahead]
+        return [a for a in order if a in horizon] + [a for a in order if a not in horizon]
+
+
+class _MostRecentlyUsed(O.PoolModel):
+    def eviction_order(self):
+        if self.policy != O.EVICT_LRU:
+            return super().eviction_order()
+        return sorted(super().eviction_order(), key=lambda a: -self.last_use[a])
+
+
+class _LoadOrderForLru(O.PoolModel):
+    def eviction_order(self):
+        if self.policy == O.EVICT_LRU:
+            return [a for a, n in self.refs.items() if n == 0]
+        return super().eviction_order()
+
+
+@pytest.mark.parametrize("cls", [_NearestFutureFirst, _UnrequestedLast, _MostRecentlyUsed, _LoadOrderForLru],
+                         ids=lambda c: c.__name__)
+def test_eviction_mutation_is_caught(cls):
+    from test_oracle_pins import eviction_pin_failures
+    assert eviction_pin_failures(cls) != [], f"{cls.__name__} passes the eviction pins"

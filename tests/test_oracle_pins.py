@@ -136,3 +136,58 @@ def test_pool_lifecycle_invariants():
                     assert d.m.refs == refs_before and d.m.free == free_before
             if rec[0] == "ensure" and rec[1] == O.OK:
                 assert d.m.refs[op[1]] >= 1
+
+
+def _cache_driver(model_cls=O.PoolModel, n_ad=16):
+    from pool_scenario import OracleDriver
+    return lambda pages: OracleDriver(pages, 1, n_ad, model_cls=model_cls)
+
+
+def _letters(stream):
+    return [ord(c) - ord("A") for c in stream]
+
+
+def eviction_pin_failures(model_cls=O.PoolModel):
+    """The eviction rules against what fixes them; returns a list of failures (empty = pinned).
+    (1) the introduction's two-slot sequences under LRU; (2) Belady: one request at a time,
+    farthest-future eviction gives the fewest loads any schedule can (exhaustive search);
+    (3) LRU never beats that minimum; (4) the farthest-future rule told nothing is LRU."""
+    from pool_scenario import cache_loads, min_loads
+    bad = []
+    g = json.load(open(os.path.join(GOLDEN, "eviction_toy_sequences.json")))
+    for case in g["cases"]:
+        got = cache_loads(_cache_driver(model_cls), _letters(case["stream"]), g["capacity"], O.EVICT_LRU)
+        if got != case["loads"]:
+            bad.append(f"toy {case['stream']}: {got} loads != {case['loads']}")
+    rng = np.random.default_rng(7)
+    for trial in range(120):
+        n = int(rng.integers(2, 7))
+        cap = int(rng.integers(1, n))
+        stream = rng.integers(0, n, size=int(rng.integers(1, 13))).tolist()
+        opt = min_loads(stream, cap)
+        ff = cache_loads(_cache_driver(model_cls), stream, cap, O.EVICT_FARTHEST)
+        lru = cache_loads(_cache_driver(model_cls), stream, cap, O.EVICT_LRU)
+        blind = cache_loads(_cache_driver(model_cls), stream, cap, O.EVICT_FARTHEST, foresight=False)
+        if ff != opt:
+            bad.append(f"farthest-future {ff} != optimum {opt} on {stream} (capacity {cap})")
+        if lru < opt:
+            bad.append(f"LRU {lru} below the optimum {opt} on {stream}")
+        if blind != lru:
+            bad.append(f"farthest-future without foresight {blind} != LRU {lru} on {stream}")
+    return bad
+
+
+def test_eviction_rules_pinned():
+    assert eviction_pin_failures() == []
+
+
+def test_lookahead_window():
+    """The farthest-future rule with a horizon of k requests: k = 0 or a horizon past the end of
+    the stream is the full rule; a horizon of 1 can only see the next request."""
+    from pool_scenario import cache_loads
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        stream = rng.integers(0, 6, size=30).tolist()
+        full = cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST)
+        assert cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST, lookahead=100) == full
+        assert cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST, lookahead=1) >= full
