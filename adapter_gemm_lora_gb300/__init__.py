@@ -46,7 +46,8 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_profile_enable", "lora_profile_read", "lora_linear_forward_noalloc",
             "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group",
             "lora_adapter_acquire", "lora_adapter_release", "lora_adapter_refs", "lora_pool_evict_idle",
-            "lora_adapter_ensure", "lora_pool_set_eviction"]
+            "lora_adapter_ensure", "lora_pool_set_eviction", "lora_adapter_packed_size", "lora_adapter_pack",
+            "lora_adapter_load_packed", "lora_adapter_wait"]
 KINDS = ("segments", "delta", "gemm", "scatter")
 
 
@@ -109,6 +110,10 @@ def _load():
         "lora_pool_evict_idle": (I32, [VP, I64, VP, VP, VP]),
         "lora_adapter_ensure": (I32, [VP, I32, I32, VP, VP, VP, VP, VP, VP, VP]),
         "lora_pool_set_eviction": (I32, [VP, I32, VP, I64, I32]),
+        "lora_adapter_packed_size": (I64, [VP, I32, VP]),
+        "lora_adapter_pack": (I32, [VP, I32, VP, VP, VP, I64]),
+        "lora_adapter_load_packed": (I32, [VP, I32, I32, VP, VP, I64, VP, VP]),
+        "lora_adapter_wait": (I32, [VP, I32, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -218,6 +223,47 @@ def lora_pool_set_eviction(pool, policy: int, future=None, lookahead: int = 0) -
     """Eviction rule for idle adapters; `future` = upcoming adapter requests (farthest-future rule)."""
     fut = np.ascontiguousarray(np.zeros(0) if future is None else future, dtype=np.int32)
     _check(_load().lora_pool_set_eviction(pool, policy, _ptr(fut) if fut.size else None, fut.size, lookahead))
+
+
+def _present(present, n_slots):
+    return None if present is None else np.ascontiguousarray([1 if p else 0 for p in present], dtype=np.int32)
+
+
+def lora_adapter_packed_size(pool, rank: int, present=None, n_slots: int = 0) -> int:
+    pr = _present(present, n_slots)
+    n = _load().lora_adapter_packed_size(pool, rank, _ptr(pr))
+    if n < 0:
+        raise LoraError(int(n), lora_last_error())
+    return int(n)
+
+
+def lora_adapter_pack(pool, rank: int, A_host: Sequence, B_host: Sequence, packed_host, packed_bytes: int) -> None:
+    """Pack an adapter's factors (bf16 bits; A_host[slot] [H, rank] or None) into page rows in `packed_host`."""
+    n = len(A_host)
+    keep = []
+    a_arr, b_arr = (ctypes.c_void_p * n)(), (ctypes.c_void_p * n)()
+    for i in range(n):
+        if A_host[i] is not None:
+            a = np.ascontiguousarray(A_host[i], dtype=np.uint16)
+            b = np.ascontiguousarray(B_host[i], dtype=np.uint16)
+            keep += [a, b]
+            a_arr[i], b_arr[i] = a.ctypes.data, b.ctypes.data
+    _check(_load().lora_adapter_pack(pool, rank, ctypes.cast(a_arr, ctypes.c_void_p), ctypes.cast(b_arr, ctypes.c_void_p),
+                                     _ptr(packed_host), packed_bytes))
+
+
+def lora_adapter_load_packed(pool, adapter_id: int, rank: int, packed_pinned, packed_bytes: int, n_slots: int,
+                             present=None, copy_stream=None) -> np.ndarray:
+    """Load from a packed buffer in pinned host memory on `copy_stream`, without synchronising."""
+    pr = _present(present, n_slots)
+    table = np.zeros((n_slots, 2, rank), dtype=np.int32)
+    _check(_load().lora_adapter_load_packed(pool, adapter_id, rank, _ptr(pr), _ptr(packed_pinned), packed_bytes,
+                                            _stream(copy_stream), _ptr(table)))
+    return table
+
+
+def lora_adapter_wait(pool, adapter_id: int, stream=None) -> None:
+    _check(_load().lora_adapter_wait(pool, adapter_id, _stream(stream)))
 
 
 def lora_adapter_refs(pool, adapter_id: int) -> int:

@@ -41,6 +41,10 @@ struct lora_pool {
   std::vector<int64_t> last_use;                  // per adapter id: clock of its last load / ensure / acquire
   int64_t use_clock = 0;
   int32_t evict_policy = LORA_EVICT_LOAD_ORDER;   // which idle adapter goes first
+  std::vector<cudaEvent_t> ev_ready;              // per adapter id: completion of its last packed load
+  std::vector<uint8_t> ready_pending;             // per adapter id: that load may still be in flight
+  cudaEvent_t ev_freed = nullptr;                 // recorded after every unload / eviction
+  bool freed_recorded = false;
   std::vector<int32_t> future;                    // upcoming adapter requests (farthest-future rule)
   int32_t lookahead = 0;                          // entries of `future` looked at; <= 0: all
   int64_t adapter_pages = 0;

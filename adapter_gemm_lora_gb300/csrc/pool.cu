@@ -31,6 +31,42 @@ __global__ void scatter_pages_kernel(const int32_t* __restrict__ ids, const uint
     for (int64_t v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = src[v];
   }
 }
+
+// Copy packed page rows, read straight from pinned host memory, into their pages; block 0 also
+// writes the adapter's device page table and rank.  Users of the adapter wait for the kernel
+// (an event on its stream) before reading either.
+__global__ void load_packed_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ tab_image,
+                                   const uint4* __restrict__ rows, int64_t n_pages, int32_t H,
+                                   uint4* __restrict__ pool, int32_t* __restrict__ d_tab, int32_t n_tab,
+                                   int32_t* __restrict__ d_rank, int32_t rank) {
+  const int64_t vec_per_row = H / 8;
+  for (int64_t r = blockIdx.x; r < n_pages; r += gridDim.x) {
+    const int64_t page = ids[r];
+    const uint4* src = rows + r * vec_per_row;
+    uint4* dst = pool + page * vec_per_row;
+    for (int64_t v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = src[v];
+  }
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < n_tab; i += blockDim.x) d_tab[i] = tab_image[i];
+    if (threadIdx.x == 0) *d_rank = rank;
+  }
+}
+
+// Byte layout of a packed adapter: page ids [need] int32, the device page-table image
+// [n_slots][2][64] int32, then the page rows [need][H] bf16; each part 256-byte aligned.
+struct PackedLayout {
+  int64_t need;
+  size_t ids, tab, rows, total;
+};
+PackedLayout packed_layout(const lora_pool* p, int32_t rank, int64_t n_present) {
+  PackedLayout L;
+  L.need = 2 * (int64_t)rank * n_present;
+  L.ids = 0;
+  L.tab = align_up((size_t)L.need * sizeof(int32_t), 256);
+  L.rows = L.tab + align_up((size_t)p->n_slots * kTabStride * sizeof(int32_t), 256);
+  L.total = L.rows + (size_t)L.need * p->H * sizeof(uint16_t);
+  return L;
+}
 }  // namespace
 
 int device_sm_count() {
@@ -189,6 +225,8 @@ int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slo
   p->refs.assign(max_adapters, 0);
   p->load_seq.assign(max_adapters, 0);
   p->last_use.assign(max_adapters, 0);
+  p->ev_ready.assign(max_adapters, nullptr);
+  p->ready_pending.assign(max_adapters, 0);
 
   if (!p->planning) {
     cudaError_t e = cudaGetDevice(&p->device);
@@ -216,6 +254,9 @@ void lora_pool_destroy(lora_pool* p) {
     cudaEventDestroy(r.stop);
   }
   for (auto e : p->ev_free) cudaEventDestroy(e);
+  for (auto e : p->ev_ready)
+    if (e) cudaEventDestroy(e);
+  if (p->ev_freed) cudaEventDestroy(p->ev_freed);
   if (p->d_ptab) cudaFree(p->d_ptab);
   if (p->d_rank) cudaFree(p->d_rank);
   if (p->d_err) cudaFree(p->d_err);
@@ -332,6 +373,7 @@ int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const
       for (int half = 0; half < 2; ++half)
         for (int j = 0; j < rank; ++j) dtab[(size_t)s * kTabStride + half * LORA_MAX_RANK + j] = table[((size_t)s * 2 + half) * rank + j];
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (e == cudaSuccess && p->freed_recorded) e = cudaStreamWaitEvent(st, p->ev_freed, 0);   // pages reused
     if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_stage, base, bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) {
       ProfScope prof(p, LORA_KIND_SCATTER, st);
@@ -368,10 +410,18 @@ namespace {
 int drop_adapter(lora_pool* p, int32_t aid, lora_stream_t stream, const char* who) {
   if (!p->planning) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(p->d_ptab + (size_t)aid * p->n_slots * kTabStride, 0xFF,
-                                    (size_t)p->n_slots * kTabStride * sizeof(int32_t), st);
+    cudaError_t e = cudaSuccess;
+    if (p->ready_pending[aid]) e = cudaStreamWaitEvent(st, p->ev_ready[aid], 0);   // a packed load in flight
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(p->d_ptab + (size_t)aid * p->n_slots * kTabStride, 0xFF,
+                          (size_t)p->n_slots * kTabStride * sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_rank + aid, 0, sizeof(int32_t), st);
+    // loads that reuse these pages on other streams wait for this point of `st`
+    if (e == cudaSuccess && !p->ev_freed) e = cudaEventCreateWithFlags(&p->ev_freed, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_freed, st);
     if (e != cudaSuccess) return lora_cuda_fail(e, who);
+    p->freed_recorded = true;
+    p->ready_pending[aid] = 0;
   }
   int64_t n = 0;
   for (int32_t pg : p->tables[aid]) {
@@ -486,6 +536,132 @@ int lora_adapter_release(lora_pool* p, int32_t aid) {
 int32_t lora_adapter_refs(const lora_pool* p, int32_t aid) {
   if (!p || aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0) return -1;
   return p->refs[aid];
+}
+
+int64_t lora_adapter_packed_size(const lora_pool* p, int32_t rank, const int32_t* present) {
+  if (!p || rank < 1 || rank > LORA_MAX_RANK) return (int64_t)lora_fail(LORA_EINVAL, "lora_adapter_packed_size: bad arguments");
+  int64_t n_present = 0;
+  for (int s = 0; s < p->n_slots; ++s) n_present += (!present || present[s] != 0);
+  return (int64_t)packed_layout(p, rank, n_present).total;
+}
+
+int lora_adapter_pack(const lora_pool* p, int32_t rank, const void* const* A_host, const void* const* B_host,
+                      void* packed, int64_t packed_bytes) {
+  if (!p || rank < 1 || rank > LORA_MAX_RANK || !A_host || !B_host || !packed)
+    return lora_fail(LORA_EINVAL, "lora_adapter_pack: bad arguments");
+  int64_t n_present = 0;
+  for (int s = 0; s < p->n_slots; ++s) {
+    if (!A_host[s]) continue;
+    if (!B_host[s]) return lora_fail(LORA_EINVAL, "lora_adapter_pack: B_host[slot] is NULL where A_host[slot] is set");
+    ++n_present;
+  }
+  const PackedLayout PL = packed_layout(p, rank, n_present);
+  if (packed_bytes < (int64_t)PL.total)
+    return lora_fail(LORA_EINVAL, "lora_adapter_pack: buffer has " + std::to_string(packed_bytes) + " bytes, needs " +
+                                      std::to_string(PL.total));
+  const int64_t H = p->H;
+  uint16_t* rows = reinterpret_cast<uint16_t*>(static_cast<char*>(packed) + PL.rows);
+  int64_t r = 0;
+  for (int s = 0; s < p->n_slots; ++s) {
+    if (!A_host[s]) continue;
+    const uint16_t* A = static_cast<const uint16_t*>(A_host[s]);
+    const uint16_t* B = static_cast<const uint16_t*>(B_host[s]);
+    for (int j = 0; j < rank; ++j, ++r)          // column j of A (H x rank, row-major)
+      for (int64_t k = 0; k < H; ++k) rows[r * H + k] = A[k * rank + j];
+    for (int j = 0; j < rank; ++j, ++r)          // row j of B (rank x H, row-major)
+      std::memcpy(rows + r * H, B + (int64_t)j * H, H * sizeof(uint16_t));
+  }
+  return LORA_OK;
+}
+
+int lora_adapter_load_packed(lora_pool* p, int32_t aid, int32_t rank, const int32_t* present, const void* packed,
+                             int64_t packed_bytes, lora_stream_t copy_stream, int32_t* table_out) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: pool is NULL");
+  if (p->planning) return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: planning pool has no device state");
+  if (aid < 0 || aid >= p->max_adapters)
+    return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: adapter id " + std::to_string(aid) + " outside [0, max_adapters)");
+  if (rank < 1 || rank > LORA_MAX_RANK)
+    return lora_fail(LORA_ERANK, "lora_adapter_load_packed: rank " + std::to_string(rank) + " outside [1, 64]");
+  if (p->rank[aid] != 0)
+    return lora_fail(LORA_EEXIST, "lora_adapter_load_packed: adapter " + std::to_string(aid) + " already loaded");
+  if (!packed || (reinterpret_cast<uintptr_t>(packed) & 15) != 0)
+    return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: packed buffer must be 16-byte aligned");
+  const int S = p->n_slots;
+  int64_t n_present = 0;
+  for (int s = 0; s < S; ++s) n_present += (!present || present[s] != 0);
+  const PackedLayout PL = packed_layout(p, rank, n_present);
+  if (packed_bytes < (int64_t)PL.total)
+    return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: buffer has " + std::to_string(packed_bytes) +
+                                      " bytes, needs " + std::to_string(PL.total));
+  void* dptr = nullptr;
+  if (cudaHostGetDevicePointer(&dptr, const_cast<void*>(packed), 0) != cudaSuccess || !dptr) {
+    cudaGetLastError();
+    return lora_fail(LORA_EINVAL, "lora_adapter_load_packed: packed buffer is not pinned host memory");
+  }
+  if (PL.need > (int64_t)p->free_list.size())
+    return lora_fail(LORA_ENOPAGES, "lora_adapter_load_packed: adapter needs " + std::to_string(PL.need) + " pages, " +
+                                        std::to_string(p->free_list.size()) + " free");
+  // Take pages as lora_adapter_load does and write the header the kernel reads.
+  char* host = static_cast<char*>(const_cast<void*>(packed));
+  int32_t* ids = reinterpret_cast<int32_t*>(host + PL.ids);
+  int32_t* tab_image = reinterpret_cast<int32_t*>(host + PL.tab);
+  std::vector<int32_t> table((size_t)S * 2 * rank, -1);
+  std::vector<int32_t> taken;
+  taken.reserve(PL.need);
+  for (int i = 0; i < S * kTabStride; ++i) tab_image[i] = -1;
+  for (int s = 0; s < S; ++s) {
+    if (present && present[s] == 0) continue;
+    for (int half = 0; half < 2; ++half)
+      for (int j = 0; j < rank; ++j) {
+        const int32_t pg = p->free_list.back();
+        p->free_list.pop_back();
+        table[((size_t)s * 2 + half) * rank + j] = pg;
+        tab_image[s * kTabStride + half * LORA_MAX_RANK + j] = pg;
+        ids[taken.size()] = pg;
+        taken.push_back(pg);
+      }
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(copy_stream);
+  cudaError_t e = cudaSuccess;
+  if (p->freed_recorded) e = cudaStreamWaitEvent(st, p->ev_freed, 0);      // reused pages are no longer read
+  if (e == cudaSuccess && !p->ev_ready[aid]) e = cudaEventCreateWithFlags(&p->ev_ready[aid], cudaEventDisableTiming);
+  if (e == cudaSuccess) {
+    ProfScope prof(p, LORA_KIND_SCATTER, st);
+    const char* dbase = static_cast<const char*>(dptr);
+    const int grid = (int)std::min<int64_t>(std::max<int64_t>(PL.need, 1), 4 * (int64_t)device_sm_count());
+    load_packed_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const int32_t*>(dbase + PL.ids),
+                                              reinterpret_cast<const int32_t*>(dbase + PL.tab),
+                                              reinterpret_cast<const uint4*>(dbase + PL.rows), PL.need, p->H,
+                                              reinterpret_cast<uint4*>(p->pool_dev),
+                                              p->d_ptab + (size_t)aid * S * kTabStride, S * kTabStride, p->d_rank + aid,
+                                              rank);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(p->ev_ready[aid], st);
+  if (e != cudaSuccess) {
+    for (auto it = taken.rbegin(); it != taken.rend(); ++it) p->free_list.push_back(*it);
+    return lora_cuda_fail(e, "lora_adapter_load_packed");
+  }
+  for (int32_t pg : taken) p->page_state[pg] = 2;
+  p->rank[aid] = rank;
+  p->refs[aid] = 0;
+  p->load_seq[aid] = p->next_seq++;
+  p->last_use[aid] = ++p->use_clock;
+  p->tables[aid] = table;
+  p->adapter_pages += PL.need;
+  p->resident += 1;
+  p->ready_pending[aid] = 1;
+  if (table_out) std::memcpy(table_out, table.data(), table.size() * sizeof(int32_t));
+  return LORA_OK;
+}
+
+int lora_adapter_wait(lora_pool* p, int32_t aid, lora_stream_t stream) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_adapter_wait: pool is NULL");
+  if (aid < 0 || aid >= p->max_adapters || p->rank[aid] == 0)
+    return lora_fail(LORA_EUNKNOWN_ADAPTER, "lora_adapter_wait: adapter " + std::to_string(aid) + " is not loaded");
+  if (p->planning || !p->ready_pending[aid]) return LORA_OK;
+  cudaError_t e = cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), p->ev_ready[aid], 0);
+  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "lora_adapter_wait");
 }
 
 int lora_pool_evict_idle(lora_pool* p, int64_t need, lora_stream_t stream, int32_t* evicted_host, int32_t* n_evicted) {

@@ -150,6 +150,35 @@ int lora_adapter_load(lora_pool* pool, int32_t adapter_id, int32_t rank,
                       const void* const* A_host, const void* const* B_host,
                       lora_stream_t stream, int32_t* page_table_host);
 
+/*
+ * Loads that overlap compute ("S-LoRA, in depth", "Scheduling": the prefetcher copies the next
+ * batch's adapters while the current batch computes; pinned host memory and a separate copy
+ * stream make the overlap possible).  An adapter is packed once, on the host, into page rows in
+ * the order lora_adapter_load takes pages (slot, A columns then B rows, j ascending), behind a
+ * header the load fills in; the caller keeps the packed form in pinned (page-locked) host memory.
+ *   lora_adapter_packed_size: bytes of the packed form for `rank` on the slots marked in
+ *     present_host (nullable int32 [n_slots], non-zero = LoRA on that slot; NULL = every slot).
+ *   lora_adapter_pack: host only; A_host / B_host as for lora_adapter_load (NULL A = no LoRA
+ *     on that slot, which must agree with present_host at load time).
+ *   lora_adapter_load_packed: takes the adapter's pages at once (host bookkeeping, same order
+ *     and errors as lora_adapter_load) and enqueues on `copy_stream` one kernel that reads the
+ *     packed rows straight from the pinned buffer into those pages and writes the adapter's
+ *     device page table and rank; it does not synchronise.  Before reusing pages it makes
+ *     copy_stream wait for the last unload or eviction, so batches enqueued before that still
+ *     read the old contents.  The buffer must be pinned host memory (LORA_EINVAL otherwise),
+ *     16-byte aligned, and unchanged until copy_stream has passed the load.
+ *   lora_adapter_wait: makes `stream` wait for the adapter's last packed load (no-op after a
+ *     synchronous load); work on `stream` that uses the adapter must come after it.
+ * Unload and eviction of an adapter whose packed load may be in flight wait for it first.
+ */
+int64_t lora_adapter_packed_size(const lora_pool* pool, int32_t rank, const int32_t* present_host);
+int lora_adapter_pack(const lora_pool* pool, int32_t rank, const void* const* A_host, const void* const* B_host,
+                      void* packed_host, int64_t packed_bytes);
+int lora_adapter_load_packed(lora_pool* pool, int32_t adapter_id, int32_t rank, const int32_t* present_host,
+                             const void* packed_pinned, int64_t packed_bytes, lora_stream_t copy_stream,
+                             int32_t* page_table_host);
+int lora_adapter_wait(lora_pool* pool, int32_t adapter_id, lora_stream_t stream);
+
 /* Return an adapter's pages to the free list (in the order they were taken) and clear its
  * device page table (enqueued on `stream`; work already enqueued before it on that stream
  * still sees the adapter).  LORA_EUNKNOWN_ADAPTER if it is not loaded, LORA_EBUSY if it has

@@ -317,3 +317,39 @@ def test_eviction_sim_tool_runs(L):
     assert set(out["policies"]) == {"load_order", "lru", "farthest_k2", "farthest_full_window"}
     for rec in out["policies"].values():
         assert 0 < rec["loads_per_request"] <= 1
+
+
+def test_packed_adapter_rows_follow_the_page_order(L):
+    """lora_adapter_pack (host only) writes A's columns and B's rows per slot in the order the
+    pool takes pages: the packed rows equal the oracle's pool read through its page table."""
+    H, S, r = 128, 3, 5
+    pool = L.lora_pool_create(None, 64, H, S, 2)
+    try:
+        rng = np.random.default_rng(12)
+        A = [rng.integers(0, 2**16, size=(H, r), dtype=np.uint16), None, rng.integers(0, 2**16, size=(H, r), dtype=np.uint16)]
+        B = [rng.integers(0, 2**16, size=(r, H), dtype=np.uint16), None, rng.integers(0, 2**16, size=(r, H), dtype=np.uint16)]
+        present = [a is not None for a in A]
+        nbytes = L.lora_adapter_packed_size(pool, r, present, S)
+        need = 2 * r * 2
+        header = -(-need * 4 // 256) * 256 + -(-S * 128 * 4 // 256) * 256
+        assert nbytes == header + need * H * 2
+        need_all = 2 * r * S                                  # every slot present
+        assert L.lora_adapter_packed_size(pool, r) == \
+            -(-need_all * 4 // 256) * 256 + -(-S * 128 * 4 // 256) * 256 + need_all * H * 2
+        buf = np.zeros(nbytes, dtype=np.uint8)
+        L.lora_adapter_pack(pool, r, A, B, buf, nbytes)
+        rows = buf[header:].view(np.uint16).reshape(need, H)
+        model = O.PoolModel(64, S, 2)
+        st, tab = model.load(0, r, present)
+        opool = np.zeros((64, H), np.uint16)
+        O.place_adapter(opool, tab, A, B)
+        order = [int(p) for s in range(S) for half in (0, 1) for p in tab[s, half] if p >= 0]
+        assert np.array_equal(rows, opool[order])
+        with pytest.raises(L.LoraError) as e:
+            L.lora_adapter_pack(pool, r, A, B, buf, nbytes - 1)
+        assert e.value.code == L.LORA_EINVAL
+        with pytest.raises(L.LoraError) as e:                 # planning pool: no device
+            L.lora_adapter_load_packed(pool, 0, r, buf, nbytes, S, present=present, copy_stream=0)
+        assert e.value.code == L.LORA_EINVAL
+    finally:
+        L.lora_pool_destroy(pool)

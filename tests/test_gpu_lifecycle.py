@@ -100,3 +100,96 @@ def test_evict_and_reload_in_stream_order(L):
         assert [L.lora_adapter_refs(pool, a) for a in range(n_ad)] == [model.refs.get(a, -1) for a in range(n_ad)]
     finally:
         L.lora_pool_destroy(pool)
+
+
+def test_packed_loads_on_a_copy_stream(L):
+    """Adapters packed into pinned host memory and loaded on a copy stream ("Scheduling":
+    prefetch on a separate stream from pinned memory) give the same pages, page contents and
+    outputs, bit for bit, as synchronous loads; a packed load into the pages of an adapter just
+    unloaded behind a queued batch leaves that batch's result intact."""
+    import torch
+    H, T, S = 512, 80, 2
+    ranks = [8, 64, 16, 3, 32, 40]
+    n_ad = len(ranks)
+    wl = workloads.small(H=H, T=T, n_adapters=n_ad, ranks=ranks, seed=77, n_slots=S, kv_fill=0.0)
+    present = {a: [True, a % 2 == 0] for a in range(n_ad)}          # odd adapters carry no LoRA on slot 1
+    pages = {a: 2 * ranks[a] * sum(present[a]) for a in range(n_ad)}
+    num_pages = sum(pages[a] for a in range(5)) + 8
+    order = np.random.default_rng(78).permutation(num_pages)
+    pool_ts = [torch.full((num_pages, H), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    p_sync = L.lora_pool_create(pool_ts[0], num_pages, H, S, n_ad, order)
+    p_pack = L.lora_pool_create(pool_ts[1], num_pages, H, S, n_ad, order)
+    model = O.PoolModel(num_pages, S, n_ad, order)
+    opool = np.full((num_pages, H), 0x7FC0, np.uint16)
+    copy = torch.cuda.Stream()
+    bufs = {}
+
+    def factors(a):
+        return ([wl.A(a, s) if present[a][s] else None for s in range(S)],
+                [wl.B(a, s) if present[a][s] else None for s in range(S)])
+
+    def load_packed(a):
+        A, B = factors(a)
+        nbytes = L.lora_adapter_packed_size(p_pack, ranks[a], present[a], S)
+        buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        L.lora_adapter_pack(p_pack, ranks[a], A, B, buf, nbytes)
+        bufs[a] = buf                                   # kept until the copy stream has passed the load
+        tab = L.lora_adapter_load_packed(p_pack, a, ranks[a], buf, nbytes, S, present=present[a], copy_stream=copy)
+        st, mtab = model.load(a, ranks[a], present[a])
+        assert st == O.OK and np.array_equal(tab.astype(np.int64), mtab), f"page table of adapter {a}"
+        O.place_adapter(opool, mtab, A, B)
+
+    def forward(pool, ta, slot):
+        nbytes = L.lora_segments_size(pool, T)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        seg = L.lora_segments_init(pool, ws, nbytes, T)
+        ta_t = torch.from_numpy(ta).cuda()
+        L.lora_segments_build(pool, ta_t, T, seg)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        d = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        L.lora_linear_forward(pool, seg, slot, bits_to_torch(wl.x(slot)), bits_to_torch(wl.W(slot)), y, d)
+        return y, d, (ws, ta_t)
+
+    try:
+        for a in range(5):
+            A, B = factors(a)
+            L.lora_adapter_load(p_sync, a, ranks[a], A, B, S)
+            load_packed(a)
+        cur = torch.cuda.current_stream()
+        for a in range(5):
+            L.lora_adapter_wait(p_pack, a, cur)
+        rng = np.random.default_rng(79)
+        ta = rng.choice(np.array([-1, 0, 1, 2, 3, 4], dtype=np.int32), size=T).astype(np.int32)
+        for slot in range(S):
+            ys, ds, _ = forward(p_sync, ta, slot)
+            yp, dp, _ = forward(p_pack, ta, slot)
+            torch.cuda.synchronize()
+            assert np.array_equal(torch_to_bits(ys), torch_to_bits(yp)), f"slot {slot}: y differs"
+            assert np.array_equal(ds.cpu().numpy(), dp.cpu().numpy()), f"slot {slot}: delta differs"
+            ref = O.linear_forward(opool, model.tables, ta, slot, wl.x(slot), wl.W(slot))
+            check_close(torch_to_bits(yp), dp.cpu().numpy(), ref[0], ref[1], f"packed loads, slot {slot}")
+        used = np.array(sorted(p for t in model.tables.values() for p in t.reshape(-1) if p >= 0))
+        assert torch.equal(pool_ts[0][used], pool_ts[1][used])
+        # a batch that uses adapter 1 is queued; adapter 1 is unloaded behind it and adapter 5 is
+        # loaded into its pages on the copy stream
+        tb = rng.choice(np.array([0, 1, 2], dtype=np.int32), size=T).astype(np.int32)
+        yb, db, keep = forward(p_pack, tb, 0)
+        refb = O.linear_forward(opool, {k: v.copy() for k, v in model.tables.items()}, tb, 0, wl.x(0), wl.W(0))
+        pages1 = set(model.tables[1].reshape(-1).tolist()) - {-1}
+        L.lora_adapter_unload(p_pack, 1)
+        assert model.unload(1) == O.OK
+        load_packed(5)
+        assert set(model.tables[5].reshape(-1).tolist()) - {-1} <= pages1
+        torch.cuda.synchronize()
+        L.lora_status(p_pack)
+        check_close(torch_to_bits(yb), db.cpu().numpy(), refb[0], refb[1], "batch queued before the page reuse")
+        L.lora_adapter_wait(p_pack, 5, cur)
+        tc = rng.choice(np.array([-1, 0, 5], dtype=np.int32), size=T).astype(np.int32)
+        yc, dc, _ = forward(p_pack, tc, 0)
+        torch.cuda.synchronize()
+        refc = O.linear_forward(opool, model.tables, tc, 0, wl.x(0), wl.W(0))
+        check_close(torch_to_bits(yc), dc.cpu().numpy(), refc[0], refc[1], "adapter packed into reclaimed pages")
+        L.lora_status(p_pack)
+    finally:
+        L.lora_pool_destroy(p_sync)
+        L.lora_pool_destroy(p_pack)
