@@ -47,7 +47,8 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_segments_size_group", "lora_segments_init_group", "lora_linear_forward_group",
             "lora_adapter_acquire", "lora_adapter_release", "lora_adapter_refs", "lora_pool_evict_idle",
             "lora_adapter_ensure", "lora_pool_set_eviction", "lora_adapter_packed_size", "lora_adapter_pack",
-            "lora_adapter_load_packed", "lora_adapter_wait"]
+            "lora_adapter_load_packed", "lora_adapter_wait", "lora_kv_grow", "lora_kv_free", "lora_kv_length",
+            "lora_kv_table"]
 KINDS = ("segments", "delta", "gemm", "scatter")
 
 
@@ -114,6 +115,10 @@ def _load():
         "lora_adapter_pack": (I32, [VP, I32, VP, VP, VP, I64]),
         "lora_adapter_load_packed": (I32, [VP, I32, I32, VP, VP, I64, VP, VP]),
         "lora_adapter_wait": (I32, [VP, I32, VP]),
+        "lora_kv_grow": (I32, [VP, I64, I32, I32, VP]),
+        "lora_kv_free": (I32, [VP, I64]),
+        "lora_kv_length": (I64, [VP, I64]),
+        "lora_kv_table": (I32, [VP, I64, I32, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -264,6 +269,31 @@ def lora_adapter_load_packed(pool, adapter_id: int, rank: int, packed_pinned, pa
 
 def lora_adapter_wait(pool, adapter_id: int, stream=None) -> None:
     _check(_load().lora_adapter_wait(pool, adapter_id, _stream(stream)))
+
+
+def lora_kv_grow(pool, request_id: int, n_tokens: int, layers: int) -> list:
+    """KV pages for n_tokens new tokens of a request (2 * layers per token); returns their ids."""
+    ids = np.zeros(max(2 * layers * n_tokens, 1), dtype=np.int32)
+    _check(_load().lora_kv_grow(pool, request_id, n_tokens, layers, _ptr(ids)))
+    return ids[:2 * layers * n_tokens].tolist()
+
+
+def lora_kv_free(pool, request_id: int) -> None:
+    _check(_load().lora_kv_free(pool, request_id))
+
+
+def lora_kv_length(pool, request_id: int) -> int:
+    return int(_load().lora_kv_length(pool, request_id))
+
+
+def lora_kv_table(pool, request_id: int, layer: int) -> np.ndarray:
+    """int32 [tokens, 2]: the (K page, V page) of every cached token of a request at one layer."""
+    n = lora_kv_length(pool, request_id)
+    if n < 0:
+        raise LoraError(LORA_EINVAL, f"request {request_id} holds no KV pages")
+    out = np.zeros((max(n, 1), 2), dtype=np.int32)
+    _check(_load().lora_kv_table(pool, request_id, layer, _ptr(out)))
+    return out[:n]
 
 
 def lora_adapter_refs(pool, adapter_id: int) -> int:

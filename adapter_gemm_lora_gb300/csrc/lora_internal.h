@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/lora.h"
@@ -32,7 +33,7 @@ struct lora_pool {
 
   // host bookkeeping
   std::vector<int32_t> free_list;                 // taken from the back
-  std::vector<uint8_t> page_state;                // 0 free, 1 reserved, 2 adapter
+  std::vector<uint8_t> page_state;                // 0 free, 1 reserved, 2 adapter, 4 KV of a request
   std::vector<int32_t> rank;                      // per adapter id; 0 = not loaded
   std::vector<std::vector<int32_t>> tables;       // per adapter id: [n_slots][2][rank]
   std::vector<int32_t> refs;                      // per adapter id: active requests
@@ -45,6 +46,11 @@ struct lora_pool {
   std::vector<uint8_t> ready_pending;             // per adapter id: that load may still be in flight
   cudaEvent_t ev_freed = nullptr;                 // recorded after every unload / eviction
   bool freed_recorded = false;
+  struct KVReq {
+    int32_t layers = 0;
+    std::vector<int32_t> pages;                   // per token: per layer, K page then V page
+  };
+  std::unordered_map<int64_t, KVReq> kv;          // request id -> its KV pages
   std::vector<int32_t> future;                    // upcoming adapter requests (farthest-future rule)
   int32_t lookahead = 0;                          // entries of `future` looked at; <= 0: all
   int64_t adapter_pages = 0;

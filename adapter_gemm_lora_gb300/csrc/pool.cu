@@ -279,6 +279,63 @@ int lora_pool_reserve(lora_pool* p, int64_t n, int64_t* ids) {
   return LORA_OK;
 }
 
+int lora_kv_grow(lora_pool* p, int64_t request, int32_t n_tokens, int32_t layers, int32_t* ids_out) {
+  if (!p || n_tokens < 0 || layers < 1) return lora_fail(LORA_EINVAL, "lora_kv_grow: bad arguments");
+  auto it = p->kv.find(request);
+  if (it != p->kv.end() && it->second.layers != layers)
+    return lora_fail(LORA_EINVAL, "lora_kv_grow: request " + std::to_string(request) + " has " +
+                                      std::to_string(it->second.layers) + " layers");
+  const int64_t need = 2 * (int64_t)layers * n_tokens;
+  if (need > (int64_t)p->free_list.size())
+    return lora_fail(LORA_ENOPAGES, "lora_kv_grow: " + std::to_string(need) + " pages asked, " +
+                                        std::to_string(p->free_list.size()) + " free");
+  auto& req = p->kv[request];
+  req.layers = layers;
+  for (int64_t i = 0; i < need; ++i) {
+    const int32_t pg = p->free_list.back();
+    p->free_list.pop_back();
+    p->page_state[pg] = 4;
+    req.pages.push_back(pg);
+    if (ids_out) ids_out[i] = pg;
+  }
+  p->reserved_pages += need;
+  return LORA_OK;
+}
+
+int lora_kv_free(lora_pool* p, int64_t request) {
+  if (!p) return lora_fail(LORA_EINVAL, "lora_kv_free: pool is NULL");
+  auto it = p->kv.find(request);
+  if (it == p->kv.end()) return lora_fail(LORA_EINVAL, "lora_kv_free: request " + std::to_string(request) + " holds no pages");
+  for (int32_t pg : it->second.pages) {
+    p->page_state[pg] = 0;
+    p->free_list.push_back(pg);
+  }
+  p->reserved_pages -= (int64_t)it->second.pages.size();
+  p->kv.erase(it);
+  return LORA_OK;
+}
+
+int64_t lora_kv_length(const lora_pool* p, int64_t request) {
+  if (!p) return -1;
+  auto it = p->kv.find(request);
+  if (it == p->kv.end()) return -1;
+  return (int64_t)it->second.pages.size() / (2 * it->second.layers);
+}
+
+int lora_kv_table(const lora_pool* p, int64_t request, int32_t layer, int32_t* table) {
+  if (!p || !table) return lora_fail(LORA_EINVAL, "lora_kv_table: bad arguments");
+  auto it = p->kv.find(request);
+  if (it == p->kv.end()) return lora_fail(LORA_EINVAL, "lora_kv_table: request " + std::to_string(request) + " holds no pages");
+  const int32_t L = it->second.layers;
+  if (layer < 0 || layer >= L) return lora_fail(LORA_EINVAL, "lora_kv_table: layer out of range");
+  const int64_t n = (int64_t)it->second.pages.size() / (2 * L);
+  for (int64_t t = 0; t < n; ++t) {
+    table[2 * t] = it->second.pages[(t * L + layer) * 2];
+    table[2 * t + 1] = it->second.pages[(t * L + layer) * 2 + 1];
+  }
+  return LORA_OK;
+}
+
 int lora_pool_release(lora_pool* p, int64_t n, const int64_t* ids) {
   if (!p || n < 0 || (n > 0 && !ids)) return lora_fail(LORA_EINVAL, "lora_pool_release: bad arguments");
   int64_t i = 0;

@@ -64,7 +64,7 @@ typedef struct lora_pool_stats_t {
   int64_t num_pages;
   int64_t free_pages;
   int64_t adapter_pages;
-  int64_t reserved_pages;      /* KV / filler pages taken by lora_pool_reserve */
+  int64_t reserved_pages;      /* KV / filler pages: lora_pool_reserve and lora_kv_grow */
   int32_t resident_adapters;
   int32_t max_adapters;
 } lora_pool_stats_t;
@@ -128,6 +128,29 @@ int lora_pool_create(void* pool_dev, int64_t num_pages, int32_t H, int32_t n_slo
  * grow_kv).  page_ids_host (int64 [n], out) receives them in the order taken.
  * LORA_ENOPAGES if fewer than n are free (nothing taken). */
 int lora_pool_reserve(lora_pool* pool, int64_t n, int64_t* page_ids_host);
+
+/*
+ * KV-cache pages of a request ("Unified paging": a sequence of length S takes S pages per K and
+ * per V; the pool sketch's grow_kv takes 2 * layers pages for each new token, from the same free
+ * list as adapter pages).
+ *   lora_kv_grow: n_tokens new tokens of `request_id` (any int64 key); each takes 2 * layers
+ *     pages from the end of the free list, per layer ascending its K page then its V page.
+ *     page_ids_host (nullable, out: int32 [n_tokens * 2 * layers]) receives them in that order.
+ *     LORA_ENOPAGES if fewer are free (nothing taken: the caller preempts or aborts, as in the
+ *     sketch); LORA_EINVAL for n_tokens < 0, layers < 1, or a layer count that differs from the
+ *     request's first growth.
+ *   lora_kv_free: a finished request gives every KV page back, in the order taken
+ *     (LORA_EINVAL if the request holds none).
+ *   lora_kv_length: the request's cached tokens, or -1 if it holds no pages.
+ *   lora_kv_table: table_host (out: int32 [tokens][2]) = (K page, V page) of every cached token
+ *     at `layer`, in token order.
+ * These are host bookkeeping; they count as reserved pages in lora_pool_stats and cannot be
+ * given back through lora_pool_release.
+ */
+int lora_kv_grow(lora_pool* pool, int64_t request_id, int32_t n_tokens, int32_t layers, int32_t* page_ids_host);
+int lora_kv_free(lora_pool* pool, int64_t request_id);
+int64_t lora_kv_length(const lora_pool* pool, int64_t request_id);
+int lora_kv_table(const lora_pool* pool, int64_t request_id, int32_t layer, int32_t* table_host);
 
 /* Give back n reserved pages (appended to the free list in the order given).
  * LORA_EINVAL if any id is not currently reserved or appears twice (nothing released). */

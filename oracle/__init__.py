@@ -2,4 +2,4 @@
 from .lora_oracle import (OK, EINVAL, ENOPAGES, EUNKNOWN_ADAPTER, ERANK, EEXIST, EBUSY, MAX_RANK,  # noqa: F401
                           EVICT_LOAD_ORDER, EVICT_LRU, EVICT_FARTHEST,
                           PoolModel, bf16_to_f64, bf16_round, gather_adapter, linear_forward, place_adapter,
-                          merged_forward, segments)
+                          merged_forward, segments, attention_decode)

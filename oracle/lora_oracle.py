@@ -107,6 +107,8 @@ class PoolModel:
         self.lookahead = 0                      # requests of `future` looked at (<= 0: all)
         self.clock = 0
         self.last_use: Dict[int, int] = {}
+        self.kv: Dict[int, List[int]] = {}      # request -> its KV pages, in the order taken
+        self.kv_layers: Dict[int, int] = {}
 
     @staticmethod
     def pages_for_adapter(rank: int, layers: int, projections: int) -> int:
@@ -256,9 +258,40 @@ class PoolModel:
         self.refs[adapter] = 1
         return OK, table, True, evicted
 
+    # ---- KV cache pages per request: the sketch's grow_kv ----
+    def kv_grow(self, request: int, n_tokens: int, layers: int):
+        """Pages for n_tokens new tokens of a request: each token takes 2 * layers pages (per
+        layer ascending, its K vector then its V vector), popped from the shared free list.  Too
+        few free pages: ENOPAGES, nothing taken (the sketch's "caller must preempt or abort").
+        A request keeps the layer count of its first growth."""
+        if n_tokens < 0 or layers < 1 or (request in self.kv_layers and self.kv_layers[request] != layers):
+            return EINVAL, None
+        need = 2 * layers * n_tokens
+        if need > len(self.free):
+            return ENOPAGES, None
+        ids = [self.free.pop() for _ in range(need)]
+        self.kv.setdefault(request, []).extend(ids)
+        self.kv_layers[request] = layers
+        return OK, ids
+
+    def kv_free(self, request: int) -> int:
+        """A finished request gives all its KV pages back, in the order they were taken."""
+        if request not in self.kv:
+            return EINVAL
+        self.free.extend(self.kv.pop(request))
+        self.kv_layers.pop(request)
+        return OK
+
+    def kv_table(self, request: int, layer: int) -> np.ndarray:
+        """int [tokens, 2]: the (K page, V page) of every cached token of the request at a layer."""
+        L = self.kv_layers[request]
+        ids = np.asarray(self.kv[request], dtype=np.int64).reshape(-1, L, 2)
+        return ids[:, layer, :]
+
     def stats(self) -> dict:
         adapter_pages = sum(int((t >= 0).sum()) for t in self.tables.values())
-        return {"free": len(self.free), "adapter": adapter_pages, "reserved": len(self.reserved),
+        kv_pages = sum(len(v) for v in self.kv.values())
+        return {"free": len(self.free), "adapter": adapter_pages, "reserved": len(self.reserved) + kv_pages,
                 "resident_adapters": len(self.tables)}
 
 
@@ -370,3 +403,39 @@ def bf16_round(values: np.ndarray) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
     return bf16_to_f64(u.astype(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# Decode attention over KV pages of the same pool
+# ---------------------------------------------------------------------------
+def attention_decode(pool_bits: np.ndarray, kv_tables: Sequence[np.ndarray], q_bits: np.ndarray,
+                     n_heads: int) -> np.ndarray:
+    """One layer's attention for one new token per request, reading K and V out of the pool.
+
+    "S-LoRA, in depth", "Unified paging": a KV cache tensor for a sequence of length S takes S
+    pages, one H-vector each, and one token holds a K and a V vector per layer; the pool serves
+    them from the same free list as adapter pages.  The pages give no attention formula; this
+    is the plain scaled dot-product attention of a decode step.  For request i, its cached
+    tokens j (K_j = pool[kv_tables[i][j, 0]], V_j = pool[kv_tables[i][j, 1]]) and each head h of
+    width d = H / n_heads:
+        s_j = q_h . K_{j,h} / sqrt(d),   p = softmax_j(s),   out_h = sum_j p_j V_{j,h}
+    q_bits: uint16 [n_req, H] bf16 bits.  Returns fp64 [n_req, H].  A request with no cached
+    token gets zeros.
+    """
+    q_all = bf16_to_f64(q_bits)
+    n_req, H = q_all.shape
+    d = H // n_heads
+    out = np.zeros((n_req, H))
+    for i in range(n_req):
+        tab = np.asarray(kv_tables[i], dtype=np.int64)
+        if tab.shape[0] == 0:
+            continue
+        K = bf16_to_f64(pool_bits[tab[:, 0]])
+        V = bf16_to_f64(pool_bits[tab[:, 1]])
+        for h in range(n_heads):
+            cols = slice(h * d, (h + 1) * d)
+            s = np.array([float(np.dot(q_all[i, cols], K[j, cols])) for j in range(tab.shape[0])]) / np.sqrt(d)
+            w = np.exp(s - s.max())
+            w /= w.sum()
+            out[i, cols] = w @ V[:, cols]
+    return out

@@ -39,6 +39,16 @@ class OracleDriver:
     def set_eviction(self, policy, future=(), lookahead=0):
         return self.m.set_eviction(policy, future, lookahead)
 
+    def kv_grow(self, req, n, layers):
+        st, ids = self.m.kv_grow(req, n, layers)
+        return st, ids
+
+    def kv_free(self, req):
+        return self.m.kv_free(req)
+
+    def kv_table(self, req, layer):
+        return self.m.kv_table(req, layer).tolist() if req in self.m.kv else None
+
     def refs(self, a):
         return self.m.refs.get(a, -1)
 
@@ -94,6 +104,17 @@ class LibraryDriver:
 
     def set_eviction(self, policy, future=(), lookahead=0):
         return self._call(self.L.lora_pool_set_eviction, self.p, policy, list(future), lookahead)[0]
+
+    def kv_grow(self, req, n, layers):
+        return self._call(self.L.lora_kv_grow, self.p, req, n, layers)
+
+    def kv_free(self, req):
+        return self._call(self.L.lora_kv_free, self.p, req)[0]
+
+    def kv_table(self, req, layer):
+        if self.L.lora_kv_length(self.p, req) < 0:
+            return None
+        return self.L.lora_kv_table(self.p, req, layer).tolist()
 
     def refs(self, a):
         return self.L.lora_adapter_refs(self.p, a)
@@ -180,8 +201,14 @@ def random_ops(seed, n_ops, max_adapters):
             ops.append(("release_reserved",))
         elif k < 88:
             ops.append(("unload", a))
-        elif k < 96:
+        elif k < 93:
             ops.append(("evict_idle", int(rng.integers(0, 80))))
+        elif k < 96:
+            req = int(rng.integers(0, 4))
+            if rng.random() < 0.7:
+                ops.append(("kv_grow", req, int(rng.integers(0, 4)), 1 + req % 2 + int(rng.random() < 0.05)))
+            else:
+                ops.append(("kv_free", req))
         else:
             fut = rng.integers(0, max_adapters, size=int(rng.integers(0, 20))).tolist()
             ops.append(("set_eviction", int(rng.integers(0, 3)), fut, int(rng.integers(-1, 8))))
@@ -214,6 +241,11 @@ def apply_op(driver, op, reserved_lists):
         return ("evict_idle", st, tuple(ev))
     if kind == "set_eviction":
         return ("set_eviction", driver.set_eviction(op[1], op[2], op[3]))
+    if kind == "kv_grow":
+        st, ids = driver.kv_grow(op[1], op[2], op[3])
+        return ("kv_grow", st, _freeze(ids), _freeze(driver.kv_table(op[1], 0)))
+    if kind == "kv_free":
+        return ("kv_free", driver.kv_free(op[1]))
     raise ValueError(kind)
 
 

@@ -353,3 +353,24 @@ def test_packed_adapter_rows_follow_the_page_order(L):
         assert e.value.code == L.LORA_EINVAL
     finally:
         L.lora_pool_destroy(pool)
+
+
+def test_kv_pages_match_oracle_and_release_refuses_them(L):
+    from pool_scenario import LibraryDriver, OracleDriver
+    lib, ora = LibraryDriver(L, 40, 1, 4), OracleDriver(40, 1, 4)
+    try:
+        for d in (lib, ora):
+            assert d.kv_grow(7, 2, 2) == (0, [39, 38, 37, 36, 35, 34, 33, 32])
+            assert d.kv_table(7, 1) == [[37, 36], [33, 32]]
+            assert d.kv_grow(7, 1, 3)[0] == O.EINVAL
+            assert d.kv_grow(8, 9, 2)[0] == O.ENOPAGES        # 36 asked, 32 free
+        assert L.lora_kv_length(lib.p, 7) == 2 and L.lora_kv_length(lib.p, 8) == -1
+        assert lib.stats() == ora.stats()
+        with pytest.raises(L.LoraError) as e:                # KV pages are not reserved pages
+            L.lora_pool_release(lib.p, [39])
+        assert e.value.code == L.LORA_EINVAL
+        for d in (lib, ora):
+            assert d.kv_free(7) == 0 and d.kv_free(7) == O.EINVAL
+        assert lib.stats() == ora.stats()
+    finally:
+        lib.close()

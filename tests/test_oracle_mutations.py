@@ -204,3 +204,38 @@ class _LoadOrderForLru(O.PoolModel):
 def test_eviction_mutation_is_caught(cls):
     from test_oracle_pins import eviction_pin_failures
     assert eviction_pin_failures(cls) != [], f"{cls.__name__} passes the eviction pins"
+
+
+# ---- decode attention: plausible mistakes, caught by the attention pins
+def _attention(mut):
+    def attention_decode(pool_bits, kv_tables, q_bits, n_heads):
+        q_all = L.bf16_to_f64(q_bits)
+        n_req, H = q_all.shape
+        d = H // n_heads
+        out = np.zeros((n_req, H))
+        for i in range(n_req):
+            tab = np.asarray(kv_tables[i], dtype=np.int64)
+            k_col, v_col = (1, 0) if mut == "K_V_swapped" else (0, 1)
+            K, V = L.bf16_to_f64(pool_bits[tab[:, k_col]]), L.bf16_to_f64(pool_bits[tab[:, v_col]])
+            for h in range(n_heads):
+                cols = slice(h, H, n_heads) if mut == "heads_interleaved" else slice(h * d, (h + 1) * d)
+                qs = slice(None) if mut == "scores_over_all_heads" else cols
+                s = K[:, qs] @ q_all[i, qs]
+                if mut != "no_scale":
+                    s = s / np.sqrt(d)
+                w = np.exp(s - s.max())
+                out[i, cols] = (w / w.sum()) @ V[:, cols]
+        return out
+    return attention_decode
+
+
+@pytest.mark.parametrize("mut", ["no_scale", "scores_over_all_heads", "K_V_swapped", "heads_interleaved"])
+def test_attention_mutation_is_caught(mut):
+    from test_oracle_pins import attention_pin_failures
+    assert attention_pin_failures(_attention(mut)) != [], f"{mut} passes the attention pins"
+
+
+def test_attention_restatement_passes():
+    """The same restatement without a planted mistake passes, so the pins are what catch them."""
+    from test_oracle_pins import attention_pin_failures
+    assert attention_pin_failures(_attention("none")) == []

@@ -112,7 +112,8 @@ def test_pool_lifecycle_golden_scenario():
 
 
 def test_pool_lifecycle_invariants():
-    """Random lifecycle sequences: every page is in exactly one place, only idle adapters are
+    """Random lifecycle sequences (adapters, reserved and KV pages): every page is in exactly one
+    place, only idle adapters are
     evicted, a successful ensure leaves the adapter resident with an active request, and a
     failed ensure or eviction changes nothing."""
     from pool_scenario import OracleDriver, apply_op, random_ops
@@ -125,10 +126,11 @@ def test_pool_lifecycle_invariants():
             free_before = list(d.m.free)
             rec = apply_op(d, op, reserved)
             pages = [int(p) for t in d.m.tables.values() for p in t.reshape(-1) if p >= 0]
-            assert len(pages) == len(set(pages))
-            assert not set(pages) & set(d.m.free) and not set(pages) & d.m.reserved
-            assert not set(d.m.free) & d.m.reserved
-            assert len(pages) + len(d.m.free) + len(d.m.reserved) == n_pages
+            kv = [p for ids in d.m.kv.values() for p in ids]
+            owned = pages + kv + list(d.m.reserved)
+            assert len(owned) == len(set(owned)), "a page has two owners"
+            assert not set(owned) & set(d.m.free)
+            assert len(owned) + len(d.m.free) == n_pages
             if rec[0] in ("ensure", "evict_idle"):
                 for a in rec[-1]:
                     assert refs_before.get(a) == 0, f"busy adapter {a} evicted"
@@ -191,3 +193,88 @@ def test_lookahead_window():
         full = cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST)
         assert cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST, lookahead=100) == full
         assert cache_loads(_cache_driver(), stream, 3, O.EVICT_FARTHEST, lookahead=1) >= full
+
+
+# ---- decode attention over pool pages, and the KV pages it reads -----------------------------
+def _bits(values):
+    return workloads.to_bf16_bits(np.asarray(values, dtype=np.float32))
+
+
+def attention_pin_failures(attention=None):
+    """Decode attention against closed forms; returns failures (empty = pinned)."""
+    attention = attention or O.attention_decode
+    bad = []
+    # two heads of width 4, two cached tokens with hand-picked vectors: the scores are 1, 0 (head
+    # 0) and 1, -1 (head 1) after the 1/sqrt(4) scale, so the weights are sigmoids of 1 and 2
+    H = 8
+    pool = np.zeros((6, H), np.uint16)
+    pool[2] = _bits([2, 0, 0, 0, 0, 1, 0, 0])     # K of token 0
+    pool[5] = _bits([0, 0, 0, 0, 0, -1, 0, 0])    # K of token 1
+    pool[0] = _bits([1, 1, 1, 1, 4, 0, 0, 0])     # V of token 0
+    pool[3] = _bits([3, 3, 3, 3, 0, 4, 0, 0])     # V of token 1
+    q = _bits([[1, 0, 0, 0, 0, 2, 0, 0]])
+    out = attention(pool, [np.array([[2, 0], [5, 3]])], q, 2)[0]
+    a = 1 / (1 + np.exp(-1.0))
+    b = 1 / (1 + np.exp(-2.0))
+    want = np.array([a + 3 * (1 - a)] * 4 + [4 * b, 4 * (1 - b), 0, 0])
+    if not np.allclose(out, want, rtol=0, atol=1e-12):
+        bad.append(f"two-token closed form: {out} != {want}")
+    # one cached token: the output is its V, whatever q and K are
+    rng = np.random.default_rng(3)
+    H, nh = 64, 4
+    pool = _bits(rng.standard_normal((10, H)))
+    q = _bits(rng.standard_normal((1, H)))
+    out = attention(pool, [np.array([[7, 2]])], q, nh)[0]
+    if not np.array_equal(out, O.bf16_to_f64(pool[2])):
+        bad.append("one cached token does not return its V")
+    # identical keys: uniform weights, the output is the mean of the V rows
+    tab = np.array([[7, 1], [7, 4], [7, 9]])
+    out = attention(pool, [tab], q, nh)[0]
+    if not np.allclose(out, O.bf16_to_f64(pool[[1, 4, 9]]).mean(axis=0), rtol=0, atol=1e-12):
+        bad.append("identical keys do not average V")
+    # a head sees only its own columns: changing K and q outside head 0 leaves head 0 unchanged
+    tab = np.array([[0, 1], [3, 4], [5, 6]])
+    q2 = q.copy()
+    q2[0, 16:] = _bits(rng.standard_normal(H - 16))
+    pool2 = pool.copy()
+    pool2[[0, 3, 5], 16:] = _bits(rng.standard_normal((3, H - 16)))
+    o1 = attention(pool, [tab], q, nh)[0, :16]
+    o2 = attention(pool2, [tab], q2, nh)[0, :16]
+    if not np.allclose(o1, o2, rtol=0, atol=1e-12):
+        bad.append("heads are not independent")
+    return bad
+
+
+def test_attention_decode_pinned():
+    assert attention_pin_failures() == []
+
+
+def test_attention_invariant_to_token_order_and_page_placement():
+    rng = np.random.default_rng(5)
+    H, nh, n = 128, 8, 9
+    pool = workloads.to_bf16_bits(rng.standard_normal((40, H)).astype(np.float32))
+    q = workloads.to_bf16_bits(rng.standard_normal((2, H)).astype(np.float32))
+    tabs = [rng.choice(40, size=(n, 2), replace=False), rng.choice(40, size=(4, 2), replace=False)]
+    base = O.attention_decode(pool, tabs, q, nh)
+    perm = rng.permutation(n)
+    assert np.allclose(O.attention_decode(pool, [tabs[0][perm], tabs[1]], q, nh), base, rtol=0, atol=1e-12)
+    moved = np.full_like(pool, 0x7FC0)
+    new_ids = rng.permutation(40)                       # every page moved to another id
+    moved[new_ids] = pool
+    assert np.array_equal(O.attention_decode(moved, [new_ids[t] for t in tabs], q, nh), base)
+
+
+def test_kv_pages_per_token_and_order():
+    """The sketch's grow_kv: 2 pages per layer per token (the worked example: 64 for 32 layers),
+    popped from the end of the shared free list, K then V per layer; a failed growth takes nothing."""
+    g = json.load(open(os.path.join(GOLDEN, "pool_worked_example.json")))
+    m = O.PoolModel(200, 1, 4)
+    st, ids = m.kv_grow(9, 1, g["layers"])
+    assert st == O.OK and len(ids) == g["kv_vectors_per_token"]
+    m = O.PoolModel(20, 1, 4)                           # free list 0..19, popped from the end
+    assert m.kv_grow(7, 2, 2) == (O.OK, [19, 18, 17, 16, 15, 14, 13, 12])
+    assert m.kv_table(7, 1).tolist() == [[17, 16], [13, 12]]      # layer 1: (K, V) per token
+    assert m.kv_grow(7, 1, 3)[0] == O.EINVAL            # layer count fixed by the first growth
+    assert m.kv_grow(8, 4, 2)[0] == O.ENOPAGES and len(m.free) == 12   # 16 pages asked, 12 free
+    assert m.kv_free(7) == O.OK and m.free[-8:] == [19, 18, 17, 16, 15, 14, 13, 12]
+    assert m.kv_free(7) == O.EINVAL
