@@ -113,9 +113,8 @@ def test_pool_lifecycle_golden_scenario():
 
 def test_pool_lifecycle_invariants():
     """Random lifecycle sequences (adapters, reserved and KV pages): every page is in exactly one
-    place, only idle adapters are
-    evicted, a successful ensure leaves the adapter resident with an active request, and a
-    failed ensure or eviction changes nothing."""
+    place, only idle adapters are evicted, a successful ensure leaves the adapter resident with
+    an active request, and a failed ensure or eviction changes nothing."""
     from pool_scenario import OracleDriver, apply_op, random_ops
     n_pages, n_ad = 96, 10
     for seed in range(20):
