@@ -22,10 +22,12 @@
  *  - Element types: bf16 for pool pages, x, W, y and the host A/B factors (raw 16-bit
  *    patterns); fp32 for the optional LoRA delta; int32 for token adapter ids.
  *  - Device work is enqueued on the caller's stream (a cudaStream_t passed as
- *    lora_stream_t; NULL = the legacy default stream).  Only lora_adapter_load and
- *    lora_status synchronise that stream.
+ *    lora_stream_t; NULL = the legacy default stream).  Only lora_adapter_load (also when
+ *    lora_adapter_ensure loads) and lora_status synchronise that stream.
  *  - Return value: LORA_OK (0) or a negative LORA_E* code; lora_last_error() then gives
- *    a message for the calling thread.  A failing call leaves the pool as it was.
+ *    a message for the calling thread.  A failing call leaves the pool as it was (one
+ *    exception, stated at lora_adapter_ensure: a load that fails with LORA_ECUDA after
+ *    idle adapters were evicted for it keeps those evictions).
  *  - Adapters are immutable once loaded; there is no global "active adapter": the
  *    adapter of every token travels in each call ("Switch Adapters by Routing Requests
  *    Through Resident, Verified State": request-scoped binding; an unknown adapter is
@@ -327,7 +329,8 @@ int lora_pool_evict_idle(lora_pool* pool, int64_t need, lora_stream_t stream, in
  * page order) and given one active request, and *loaded_out = 1.  table_out as for
  * lora_adapter_load; evicted_host / n_evicted as for lora_pool_evict_idle (all nullable).
  * LORA_ENOPAGES (nothing evicted, nothing loaded) if even evicting every idle adapter would
- * not free enough pages.
+ * not free enough pages; argument errors are found before anything is evicted.  If the load
+ * itself then fails with LORA_ECUDA, the evictions made for it stand.
  */
 int lora_adapter_ensure(lora_pool* pool, int32_t adapter_id, int32_t rank, const void* const* A_host,
                         const void* const* B_host, lora_stream_t stream, int32_t* table_out,
