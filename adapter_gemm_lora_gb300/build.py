@@ -60,7 +60,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 sys.stderr.write(out)
     objs = [o for o, _ in results]
     if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs])
+        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-lpthread"])
     return LIB
 
 

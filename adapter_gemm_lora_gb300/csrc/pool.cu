@@ -12,6 +12,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <thread>
 
 #include "lora_internal.h"
 
@@ -19,6 +20,53 @@ namespace {
 thread_local std::string g_last_error;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// The columns of A (H x rank, row-major) as rank page rows of H values.  Blocked over 64 rows
+// of A at a time: the block's reads stay in the first-level cache and every row receives 64
+// contiguous values per block (a column-by-column walk strides through all of A per column).
+void columns_to_rows(const uint16_t* A, int64_t H, int rank, uint16_t* rows) {
+  constexpr int64_t kBlock = 64;
+  for (int64_t k0 = 0; k0 < H; k0 += kBlock) {
+    const int64_t k1 = std::min(H, k0 + kBlock);
+    for (int j = 0; j < rank; ++j) {
+      uint16_t* dst = rows + (int64_t)j * H;
+      for (int64_t k = k0; k < k1; ++k) dst[k] = A[k * rank + j];
+    }
+  }
+}
+
+// An adapter's page rows, slot after slot (A's columns, then B's rows), into `rows`.  Slots are
+// independent, so a large adapter is split over up to 8 host threads (a host at one thread's
+// copy rate repacks a 32 MiB adapter in several ms); if a thread cannot be started, the calling
+// thread does its share.
+void pack_rows(const void* const* A_host, const void* const* B_host, const std::vector<uint8_t>& present, int64_t H,
+               int rank, uint16_t* rows) {
+  std::vector<int> slots;
+  for (int s = 0; s < (int)present.size(); ++s)
+    if (present[s]) slots.push_back(s);
+  const size_t n = slots.size();
+  auto one = [&](size_t i) {
+    const int s = slots[i];
+    uint16_t* out = rows + (int64_t)i * 2 * rank * H;
+    columns_to_rows(static_cast<const uint16_t*>(A_host[s]), H, rank, out);
+    std::memcpy(out + (int64_t)rank * H, B_host[s], (size_t)rank * H * sizeof(uint16_t));
+  };
+  unsigned nt = std::min(std::max(1u, std::thread::hardware_concurrency()), 8u);
+  if (n * 2 * rank * H * sizeof(uint16_t) < (8u << 20)) nt = 1;
+  nt = (unsigned)std::min<size_t>(nt, std::max<size_t>(n, 1));
+  auto share = [&](unsigned t) {
+    for (size_t i = t; i < n; i += nt) one(i);
+  };
+  std::vector<std::thread> threads;
+  unsigned started = 1;                          // share 0 is the calling thread's
+  try {
+    for (; started < nt; ++started) threads.emplace_back(share, started);
+  } catch (...) {
+  }
+  for (unsigned t = started; t < nt; ++t) share(t);
+  share(0);
+  for (auto& th : threads) th.join();
+}
 
 // Copy staged rows (page ids first, then the rows in the same order) into their pages.
 __global__ void scatter_pages_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ rows,
@@ -407,16 +455,7 @@ int lora_adapter_load(lora_pool* p, int32_t aid, int32_t rank, const void* const
     char* base = reinterpret_cast<char*>(p->h_stage.data());
     std::memcpy(base, taken.data(), need * sizeof(int32_t));
     uint16_t* rows = reinterpret_cast<uint16_t*>(base + ids_bytes);
-    int64_t r = 0;
-    for (int s = 0; s < S; ++s) {
-      if (!present[s]) continue;
-      const uint16_t* A = static_cast<const uint16_t*>(A_host[s]);
-      const uint16_t* B = static_cast<const uint16_t*>(B_host[s]);
-      for (int j = 0; j < rank; ++j, ++r)        // column j of A (H x rank, row-major)
-        for (int64_t k = 0; k < H; ++k) rows[r * H + k] = A[k * rank + j];
-      for (int j = 0; j < rank; ++j, ++r)        // row j of B (rank x H, row-major)
-        std::memcpy(rows + r * H, B + (int64_t)j * H, H * sizeof(uint16_t));
-    }
+    pack_rows(A_host, B_host, present, H, rank, rows);
     cudaError_t e = cudaSuccess;
     if (bytes > p->d_stage_bytes) {
       if (p->d_stage) cudaFree(p->d_stage);
@@ -618,16 +657,9 @@ int lora_adapter_pack(const lora_pool* p, int32_t rank, const void* const* A_hos
                                       std::to_string(PL.total));
   const int64_t H = p->H;
   uint16_t* rows = reinterpret_cast<uint16_t*>(static_cast<char*>(packed) + PL.rows);
-  int64_t r = 0;
-  for (int s = 0; s < p->n_slots; ++s) {
-    if (!A_host[s]) continue;
-    const uint16_t* A = static_cast<const uint16_t*>(A_host[s]);
-    const uint16_t* B = static_cast<const uint16_t*>(B_host[s]);
-    for (int j = 0; j < rank; ++j, ++r)          // column j of A (H x rank, row-major)
-      for (int64_t k = 0; k < H; ++k) rows[r * H + k] = A[k * rank + j];
-    for (int j = 0; j < rank; ++j, ++r)          // row j of B (rank x H, row-major)
-      std::memcpy(rows + r * H, B + (int64_t)j * H, H * sizeof(uint16_t));
-  }
+  std::vector<uint8_t> present(p->n_slots);
+  for (int s = 0; s < p->n_slots; ++s) present[s] = A_host[s] != nullptr;
+  pack_rows(A_host, B_host, present, H, rank, rows);
   return LORA_OK;
 }
 

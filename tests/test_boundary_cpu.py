@@ -374,3 +374,25 @@ def test_kv_pages_match_oracle_and_release_refuses_them(L):
         assert lib.stats() == ora.stats()
     finally:
         lib.close()
+
+
+def test_packing_a_large_adapter_across_threads(L):
+    """An adapter above 8 MiB is repacked by several host threads; every page row is still
+    column j of A or row j of B of its slot, slots in order (slots without LoRA skipped)."""
+    H, S, r = 2048, 40, 32
+    pool = L.lora_pool_create(None, 16, H, S, 1)
+    try:
+        rng = np.random.default_rng(21)
+        A = [None if s % 7 == 3 else rng.integers(0, 2**16, size=(H, r), dtype=np.uint16) for s in range(S)]
+        B = [None if a is None else rng.integers(0, 2**16, size=(r, H), dtype=np.uint16) for a in A]
+        present = [a is not None for a in A]
+        nbytes = L.lora_adapter_packed_size(pool, r, present, S)
+        n_rows = 2 * r * sum(present)
+        assert n_rows * H * 2 > 8 << 20
+        buf = np.zeros(nbytes, dtype=np.uint8)
+        L.lora_adapter_pack(pool, r, A, B, buf, nbytes)
+        rows = buf[nbytes - n_rows * H * 2:].view(np.uint16).reshape(-1, 2, r, H)
+        want = np.stack([np.stack([a.T, b]) for a, b in zip(A, B) if a is not None])
+        assert np.array_equal(rows, want)
+    finally:
+        L.lora_pool_destroy(pool)
