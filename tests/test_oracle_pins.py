@@ -277,3 +277,23 @@ def test_kv_pages_per_token_and_order():
     assert m.kv_grow(8, 4, 2)[0] == O.ENOPAGES and len(m.free) == 12   # 16 pages asked, 12 free
     assert m.kv_free(7) == O.OK and m.free[-8:] == [19, 18, 17, 16, 15, 14, 13, 12]
     assert m.kv_free(7) == O.EINVAL
+
+
+def test_workload_generator_scales_give_unit_variance():
+    """Sanity, not parity, on the generator the benchmark and the GPU tests draw from (the test
+    above uses the pins' own draws): with x ~ N(0,1), W, A ~ N(0, 1/H), B ~ N(0, 1/r), an
+    element of xW has variance H * 1 * (1/H) = 1 and an element of the LoRA delta (xA)B has
+    variance r * (H * 1/H) * (1/r) = 1.  A standard deviation of 1/H in place of 1/sqrt(H)
+    would give 1/H."""
+    H, T = 512, 96
+    wl = workloads.small(H=H, T=T, n_adapters=4, ranks=[8, 16, 32, 64], seed=17, none_share=0.0)
+    model = O.PoolModel(wl.spec.pool_pages, 1, 4, wl.page_order)
+    pool = np.full((wl.spec.pool_pages, H), 0x7FC0, np.uint16)
+    for a in range(4):
+        st, tab = model.load(a, int(wl.ranks[a]), [True])
+        O.place_adapter(pool, tab, [wl.A(a, 0)], [wl.B(a, 0)])
+    y, delta = O.linear_forward(pool, model.tables, wl.token_adapter, 0, wl.x(0), wl.W(0))
+    base = y - delta
+    assert 0.85 < base.var() < 1.15, base.var()
+    assert 0.8 < delta.var() < 1.2, delta.var()
+    assert abs(base.mean()) < 0.05 and abs(delta.mean()) < 0.05
