@@ -39,6 +39,7 @@ LORA_MAX_TOKENS = 65536
 LORA_MAX_GROUP = 4
 LORA_NOALLOC_MAX_TOKENS = 128
 LORA_NOALLOC_MAX_H = 8192
+LORA_NOALLOC_SCRATCH_BYTES = 17 * 1024 * 1024
 
 EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_adapter_load",
             "lora_adapter_unload", "lora_segments_size", "lora_segments_init", "lora_segments_build",

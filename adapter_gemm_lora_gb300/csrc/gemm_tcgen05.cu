@@ -17,10 +17,8 @@
 // Per CTA: one 128 x BN output tile over the full K.  Warp 0 issues TMA loads into a ring
 // of up to 8 stages (each 1, 2 or 4 K chunks of 64, so that a stage carries >= ~40 KB), warp 1 owns TMEM and a single thread issues the MMAs, then all 8 warps
 // drain TMEM (warp w reads TMEM lanes 32*(w%4) .. +31, half the columns each).
-// Token tiles shrink (down to 32 tokens) until the grid fills the SMs; CTAs that share a
-// feature tile form a thread-block cluster of up to 4 along the token dimension, and each
-// loads 1/CN of the W tile and multicasts it to the whole cluster (stages are released
-// cluster-wide by multicast tcgen05.commit), so W crosses L2 once per cluster.
+// Token tiles shrink (down to 32 tokens) until the grid fills the SMs.  Every CTA loads its own
+// W tile; CTAs that share a feature tile meet in L2, which holds W across them.
 // The epilogue stages the fp32 delta sub-tile (one TMA load) and the bf16 output (one TMA
 // store) through the freed stage memory.  The mainloop reads only x and W, so the kernel is
 // launched as a programmatic dependent of the LoRA kernels before it and waits for them
@@ -55,7 +53,7 @@ struct GemmParams {
   const int32_t* tok_adapter;
   const int32_t* ptab;
   int32_t* err;
-  int32_t T, H, BN, n_kb, kc, stages, cn, ks, slot, n_slots;
+  int32_t T, H, BN, n_kb, kc, stages, ks, slot, n_slots;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -109,16 +107,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
-}
-// The same box lands at the same shared-memory offset in every CTA of `mask` and signals each
-// CTA's mbarrier at the same offset.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                                      uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -175,13 +163,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// The same, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -368,12 +349,9 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM;
   const int t0 = blockIdx.z * p.BN;
-  const int cn = p.cn;                                  // CTAs sharing the W tile (cluster along tokens)
-  const int ks = p.ks;                                  // CTAs splitting K (cluster along x); cn == 1 then
-  const uint32_t crank = cn > 1 ? cluster_ctarank() : 0;
+  const int ks = p.ks;                                  // CTAs splitting K (cluster along x)
   const int me = ks > 1 ? (int)cluster_ctarank() : 0;   // this CTA's K slice
   const int kb0 = me * (p.n_kb / ks);                   // first 64-wide K block of the slice
-  const uint16_t cmask = (uint16_t)((1u << cn) - 1u);
   const int stages = p.stages;
   const int kc = p.kc;                                  // 64-wide K chunks per stage
   const uint32_t xb = (uint32_t)(p.BN * BK * 2);        // one x chunk
@@ -384,7 +362,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, (uint32_t)cn);      // one release per CTA of the cluster
+      mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accum, 1);
     mbar_init(bar_delta, 1);
@@ -401,17 +379,16 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (cn > 1 || ks > 1) cluster_sync_all();             // peers' barriers exist before anything targets them
+  if (ks > 1) cluster_sync_all();                       // peers' scratch blocks and barriers exist
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {                                    // TMA producer
-      const uint32_t tx = stage_bytes;                  // whole W tile (cn multicast slices) + own x tile
-      // When one cluster covers every token tile (decode batches) W crosses L2 once; otherwise
-      // other clusters re-read it, so it must not be marked for early eviction.
-      const uint64_t pol_w = (int)gridDim.z == cn ? policy_evict_first() : policy_evict_last();
+      const uint32_t tx = stage_bytes;                  // W tile + x tile
+      // When one token tile covers the batch (decode) each W tile is read once; otherwise the
+      // CTAs of the other token tiles re-read it, so it must not be marked for early eviction.
+      const uint64_t pol_w = (int)gridDim.z == 1 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_x = policy_evict_last();       // x is re-read by every feature tile
-      const int w_rows = BM / cn;
       for (int i = 0; i < nk; ++i) {
         const int s = i % stages;
         const uint32_t ph = (i / stages) & 1;
@@ -423,12 +400,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const uint32_t st = s_base + (uint32_t)s * stage_bytes;
         for (int c = 0; c < kc; ++c) {
           const int kx = (kb0 + i * kc + c) * BK;
-          const uint32_t wdst = st + (uint32_t)c * A_BYTES;
-          if (cn > 1)
-            tma_load_2d_multicast(wdst + crank * (uint32_t)(w_rows * BK * 2), &tm_w, kx, m0 + (int)crank * w_rows,
-                                  bar_full + 8 * s, cmask, pol_w);
-          else
-            tma_load_2d(wdst, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
+          tma_load_2d(st + (uint32_t)c * A_BYTES, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
           tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
         }
       }
@@ -453,10 +425,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           for (int k = 0; k < BK / 16; ++k)             // 16-element K steps = 32 bytes = 2 descriptor units
             mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
         }
-        if (cn > 1)
-          mma_commit_multicast(bar_empty + 8 * s, cmask);
-        else
-          mma_commit(bar_empty + 8 * s);
+        mma_commit(bar_empty + 8 * s);
       }
       mma_commit(bar_accum);
     }
@@ -483,7 +452,7 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     return;
   }
   pdl_wait_then_release();         // the delta and validated ids come from the kernels before this one
-  // Stage memory is free now (every multicast into it belonged to a k-block consumed above):
+  // Stage memory is free now (every load into it belonged to a k-block consumed above):
   // the fp32 delta tile [BN][128] at 0, the bf16 output tile [BN][128] after it (<= 192 KB).
   const uint32_t delta_s = s_base;
   const uint32_t y_s = s_base + (uint32_t)(p.BN * BM * 4);
@@ -528,19 +497,19 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
-  if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
 }
 
 // ---- persistent variant (batches of more than 256 tokens) ---------------------------------
-// Each cluster of cn CTAs (cn token tiles sharing one W tile, W multicast as above) walks the
-// cluster tiles c, c + n_clusters, ...  TMEM holds two accumulators of BN columns.  Warp 0 issues
+// Each CTA walks the tiles c, c + gridDim.x, ... (consecutive tiles: consecutive feature tiles of
+// one token tile, so the CTAs of a wave share x tiles in L2, and W stays in L2 across waves).
+// TMEM holds two accumulators of BN columns.  Warp 0 issues
 // TMA loads without pause across tile boundaries, warp 1 issues the MMAs of tile i into
 // accumulator i % 2, and warps 4-7 (one per TMEM lane quarter) drain accumulator (i-1) % 2
 // meanwhile: add the delta (read straight from global memory), round to bf16, store y from
 // registers.  So a tile's epilogue runs under the next tile's main loop.
 struct PersistParams {
-  int32_t m_tiles, t_groups;       // feature tiles; token-tile groups of cn tiles
-  int32_t n_ctiles;                // m_tiles * t_groups
+  int32_t m_tiles, t_tiles;        // feature tiles; token tiles
+  int32_t n_ctiles;                // m_tiles * t_tiles
 };
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -555,22 +524,18 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
   const uint32_t bar_tfull = bar_full + 16 * MAX_STAGES, bar_tempty = bar_tfull + 16;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cn = p.cn;
-  const uint32_t crank = cn > 1 ? cluster_ctarank() : 0;
-  const uint16_t cmask = (uint16_t)((1u << cn) - 1u);
   const int stages = p.stages;
   const int kc = p.kc;
   const uint32_t xb = (uint32_t)(p.BN * BK * 2);
   const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
   const int nk = p.n_kb / kc;
   const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
-  const int n_clusters = (int)gridDim.x / cn;
-  const int cluster_id = (int)blockIdx.x / cn;
+  const int n_ctas = (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, (uint32_t)cn);
+      mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
@@ -587,19 +552,17 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (cn > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {                                    // TMA producer, all tiles back to back
       const uint64_t pol_w = policy_evict_last();       // W tiles are re-read by other token tiles
       const uint64_t pol_x = policy_evict_last();       // x tiles are re-read by other feature tiles
-      const int w_rows = BM / cn;
       uint32_t it = 0;
       bool ok = true;
-      for (int ct = cluster_id; ct < pp.n_ctiles && ok; ct += n_clusters) {
+      for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int m0 = (ct % pp.m_tiles) * BM;
-        const int t0 = ((ct / pp.m_tiles) * cn + (int)crank) * p.BN;
+        const int t0 = (ct / pp.m_tiles) * p.BN;
         for (int i = 0; i < nk; ++i, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1;
@@ -612,12 +575,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
           const uint32_t st = s_base + (uint32_t)s * stage_bytes;
           for (int c = 0; c < kc; ++c) {
             const int kx = (i * kc + c) * BK;
-            const uint32_t wdst = st + (uint32_t)c * A_BYTES;
-            if (cn > 1)
-              tma_load_2d_multicast(wdst + crank * (uint32_t)(w_rows * BK * 2), &tm_w, kx, m0 + (int)crank * w_rows,
-                                    bar_full + 8 * s, cmask, pol_w);
-            else
-              tma_load_2d(wdst, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
+            tma_load_2d(st + (uint32_t)c * A_BYTES, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
             tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
           }
         }
@@ -630,7 +588,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
       uint32_t it = 0;
       int tile = 0;
       bool ok = true;
-      for (int ct = cluster_id; ct < pp.n_ctiles && ok; ct += n_clusters, ++tile) {
+      for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas, ++tile) {
         const int b = tile & 1;
         if (!mbar_wait(bar_tempty + 8 * b, ((tile >> 1) & 1) ^ 1)) {   // accumulator b drained
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
@@ -655,10 +613,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
             for (int k = 0; k < BK / 16; ++k)
               mma_bf16_ss(acc, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
           }
-          if (cn > 1)
-            mma_commit_multicast(bar_empty + 8 * s, cmask);
-          else
-            mma_commit(bar_empty + 8 * s);
+          mma_commit(bar_empty + 8 * s);
         }
         if (ok) mma_commit(bar_tfull + 8 * b);            // accumulator b complete
       }
@@ -670,10 +625,10 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
     const int row = q * 32 + lane;
     pdl_wait_then_release();                            // delta and ids come from earlier kernels
     int tile = 0;
-    for (int ct = cluster_id; ct < pp.n_ctiles; ct += n_clusters, ++tile) {
+    for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas, ++tile) {
       const int b = tile & 1;
       const int m0 = (ct % pp.m_tiles) * BM;
-      const int t0 = ((ct / pp.m_tiles) * cn + (int)crank) * p.BN;
+      const int t0 = (ct / pp.m_tiles) * p.BN;
       const int feat = m0 + row;
       bool ok = mbar_wait(bar_tfull + 8 * b, (tile >> 1) & 1);
       ok = __all_sync(0xffffffffu, ok);
@@ -720,7 +675,6 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 2 * acc_cols);
-  if (cn > 1) cluster_sync_all();                 // no peer may still signal this CTA's barriers
 }
 
 // ---- grouped split-K variant (slots that share x, batches of <= 256 tokens) --------------
@@ -1049,50 +1003,33 @@ int encode_2d_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 }  // namespace
 
 namespace {
-// Clusters of `cn` persistent CTAs that can be resident at once (cached per device and cn).
-int persistent_clusters(int cn) {
-  static int cached[64][5] = {};
+// Persistent CTAs that can be resident at once (cached per device).
+int persistent_ctas() {
+  static int cached[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev][cn] > 0) return cached[dev][cn];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cn * 64);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cn;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_lora_persistent, &cfg) != cudaSuccess || n <= 0) {
+  if (cached[dev] > 0) return cached[dev];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_lora_persistent, THREADS, SMEM_BYTES) != cudaSuccess ||
+      per_sm <= 0) {
     cudaGetLastError();
-    n = device_sm_count() / cn;
+    per_sm = 1;
   }
-  cached[dev][cn] = n;
-  return n;
+  cached[dev] = per_sm * device_sm_count();
+  return cached[dev];
 }
 }  // namespace
 
 int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_lora_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_lora_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return lora_cuda_fail(e, "gemm kernel attribute");
-    attr_set[dev] = true;
-  }
+  static DeviceFlags attr_single, attr_persist;
+  int rc0 = ensure_smem_attr(attr_single, gemm_lora_kernel, SMEM_BYTES, "gemm kernel attribute");
+  if (rc0 == LORA_OK) rc0 = ensure_smem_attr(attr_persist, gemm_lora_persistent, SMEM_BYTES, "gemm kernel attribute");
+  if (rc0 != LORA_OK) return rc0;
   const int n_sm = device_sm_count();
   const int m_tiles = (G.H + BM - 1) / BM;
   const int n_kb = G.H / BK;
-  int n_tiles, bn, cn, ks = 1;
+  int n_tiles, bn, ks = 1;
   const int ks_try = n_kb % 4 == 0 ? 4 : 2;
   const int bn_try = ((G.T + 32 * ks_try - 1) / (32 * ks_try)) * (32 * ks_try);
   if (G.T <= MAX_BN && n_kb % 2 == 0 && G.partials &&
@@ -1104,7 +1041,6 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
     ks = ks_try;
     bn = bn_try;
     n_tiles = 1;
-    cn = 1;
   } else {
     // Token tiles: as few as possible (<= 256 tokens each), but enough to fill about 3/4 of the
     // SMs when the feature tiles alone do not, down to 32-token tiles.
@@ -1116,9 +1052,6 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
     bn = ((bn + 31) / 32) * 32;
     if (bn > MAX_BN) bn = MAX_BN;
     n_tiles = (G.T + bn - 1) / bn;
-    // Wide token tiles share each W tile across a cluster (multicast); for narrow tiles the
-    // per-SM shared-memory fill rate, not L2, is the limit, and the cluster only adds coupling.
-    cn = bn < 128 ? 1 : (n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1));
   }
   // Each pipeline stage costs a fixed handshake on top of its data, and a CTA's TMA fill rate is
   // bounded, so stages are made large: up to 4 K chunks of 64, at most 96 KB (>= 2 stages).
@@ -1132,11 +1065,11 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   const int ep_rows = bn / ks;      // token rows of the delta and y tiles one CTA's epilogue moves
   // More tiles than resident CTAs: persistent CTAs overlap each tile's epilogue with the next
   // tile's main loop.
-  const int n_ctiles = m_tiles * (n_tiles / cn);
-  const int n_clusters_res = ks == 1 ? persistent_clusters(cn) : 0;
-  const bool persistent = ks == 1 && n_ctiles > n_clusters_res;
+  const int n_ctiles = m_tiles * n_tiles;
+  const int n_res = ks == 1 ? persistent_ctas() : 0;
+  const bool persistent = ks == 1 && n_ctiles > n_res;
   CUtensorMap tm_w, tm_x, tm_d, tm_y;
-  int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)(BM / cn));
+  int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)BM);
   if (rc != LORA_OK) return rc;
   rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
   if (rc != LORA_OK) return rc;
@@ -1158,30 +1091,16 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.n_kb = n_kb;
   P.kc = kc;
   P.stages = stages;
-  P.cn = cn;
   P.ks = ks;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
   if (persistent) {
     PersistParams pp;
     pp.m_tiles = m_tiles;
-    pp.t_groups = n_tiles / cn;
+    pp.t_tiles = n_tiles;
     pp.n_ctiles = n_ctiles;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_clusters_res * cn);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[2];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = cn;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = G.pdl ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_persistent, tm_w, tm_x, P, pp);
+    cudaError_t e = launch_pdl(G.pdl, gemm_lora_persistent, dim3(n_res), dim3(THREADS), SMEM_BYTES, st, tm_w, tm_x,
+                               P, pp);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
   }
@@ -1194,7 +1113,7 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = ks;
   attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = cn;
+  attrs[0].val.clusterDim.z = 1;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
@@ -1252,16 +1171,9 @@ int group_clusters() {
 
 template <int KS>
 int launch_group_ks(const GemmLaunch* G, int n, const SplitK& sk, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_lora_group_splitk<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e != cudaSuccess) return lora_cuda_fail(e, "gemm group kernel attribute");
-    attr_set[dev] = true;
-  }
+  static DeviceFlags attr;
+  int rc0 = ensure_smem_attr(attr, gemm_lora_group_splitk<KS>, SMEM_BYTES, "gemm group kernel attribute");
+  if (rc0 != LORA_OK) return rc0;
   const int H = G[0].H, T = G[0].T;
   const int m_tiles = (H + BM - 1) / BM;
   CUtensorMap tm_w[LORA_MAX_GROUP], tm_x;
@@ -1285,7 +1197,6 @@ int launch_group_ks(const GemmLaunch* G, int n, const SplitK& sk, cudaStream_t s
   P.n_kb = H / BK;
   P.kc = sk.kc;
   P.stages = sk.stages;
-  P.cn = 1;
   P.ks = KS;
   P.slot = G[0].slot;
   P.n_slots = G[0].n_slots;

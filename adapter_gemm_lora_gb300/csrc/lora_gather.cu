@@ -527,15 +527,9 @@ int active_clusters() {
 }  // namespace
 
 int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(lora_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return lora_cuda_fail(e, "lora_delta_kernel: shared memory attribute");
-    attr_set[dev] = true;
-  }
+  static DeviceFlags attr;
+  int rc = ensure_smem_attr(attr, lora_delta_kernel, kSmemBytes, "lora_delta_kernel: shared memory attribute");
+  if (rc != LORA_OK) return rc;
   // Persistent clusters, as many as can be resident; each loops over the units.
   int groups = active_clusters();
   const int item_cap = L.seg->unit_cap * L.n_group;

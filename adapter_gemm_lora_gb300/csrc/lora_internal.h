@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -21,6 +22,8 @@ enum : int32_t {
 
 // Page table entries per (adapter, slot): [2][LORA_MAX_RANK] int32.
 constexpr int kTabStride = 2 * LORA_MAX_RANK;
+// Work-list geometry shared by the segment builder and the gather kernels.
+constexpr int kUnitTokens = 16;      // tokens per LoRA-delta work unit
 
 struct lora_pool {
   void* pool_dev = nullptr;
@@ -134,9 +137,34 @@ bool gemm_group_fits(const GemmLaunch* G, int n);
 int launch_gemm_group(const GemmLaunch* G, int n, cudaStream_t st);
 // Capacity of the base GEMM's split-K scratch for a workspace of T_max tokens: 3 partial tiles
 // (4-way split) of up to 256 token columns, the tile rounded up to 128 columns.
-inline int64_t gemm_partial_floats(int32_t T_max, int32_t H) {
-  const int64_t t = T_max < 256 ? T_max : 256;
-  return 3 * ((t + 127) / 128 * 128) * (int64_t)H;
+constexpr int64_t gemm_partial_floats(int32_t T_max, int32_t H) {
+  return 3 * (((T_max < 256 ? T_max : 256) + 127) / 128 * 128) * (int64_t)H;
+}
+
+// Byte offsets of the arrays of a segment workspace (lora_segments_init) for batches of up to
+// T_max tokens, hidden size H, adapter ids below max_adapters and group calls of up to
+// max_group slots; every array starts on a 256-byte boundary.
+struct SegLayout {
+  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials, total;
+  int32_t max_seg, unit_cap;
+};
+constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+constexpr SegLayout segments_layout(int32_t T_max, int32_t H, int32_t max_adapters, int32_t max_group) {
+  SegLayout L{};
+  L.max_seg = T_max < max_adapters ? T_max : max_adapters;
+  L.unit_cap = T_max / kUnitTokens + L.max_seg + 1;
+  size_t off = 0;
+  L.perm = off;         off = align256(off + (size_t)T_max * 4);
+  L.seg_off = off;      off = align256(off + (size_t)(L.max_seg + 2) * 4);
+  L.seg_adapter = off;  off = align256(off + (size_t)(L.max_seg + 1) * 4);
+  L.n_seg = off;        off = align256(off + 16);
+  L.tok_adapter = off;  off = align256(off + (size_t)T_max * 4);
+  L.units = off;        off = align256(off + (size_t)L.unit_cap * 16);
+  L.n_units = off;      off = align256(off + 16);
+  L.delta = off;        off = align256(off + (size_t)max_group * T_max * H * 4);
+  L.partials = off;     off = align256(off + (size_t)max_group * gemm_partial_floats(T_max, H) * 4);
+  L.total = off;
+  return L;
 }
 
 // Programmatic dependent launch: every kernel of the path waits for the kernel before it
@@ -169,5 +197,23 @@ inline cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim
 
 int device_sm_count();
 
-// Work-list geometry shared by the segment builder and the gather kernels.
-constexpr int kUnitTokens = 16;      // tokens per LoRA-delta work unit
+// Kernel attributes are per device: each launcher keeps one flag per device ordinal saying that
+// its kernel's dynamic shared-memory limit has been raised there.  Setting an attribute twice is
+// harmless, so two host threads racing on a first launch both just set it.
+constexpr int kMaxDeviceFlags = 64;
+struct DeviceFlags {
+  std::atomic<bool> set[kMaxDeviceFlags] = {};
+};
+template <typename Kernel>
+int ensure_smem_attr(DeviceFlags& flags, Kernel* kernel, int bytes, const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return lora_cuda_fail(e, what);
+  const bool cached = dev >= 0 && dev < kMaxDeviceFlags;
+  if (cached && flags.set[dev].load(std::memory_order_acquire)) return LORA_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return lora_cuda_fail(e, what);
+  if (cached) flags.set[dev].store(true, std::memory_order_release);
+  return LORA_OK;
+}
+

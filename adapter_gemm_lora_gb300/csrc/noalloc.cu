@@ -22,9 +22,13 @@ namespace {
 
 constexpr int32_t kNoAllocMaxTokens = LORA_NOALLOC_MAX_TOKENS;
 constexpr int32_t kNoAllocMaxH = LORA_NOALLOC_MAX_H;
-// Segment workspace for 128 tokens at H = 8192: 4 MiB of fp32 delta, 32 KiB of s, and
-// under 32 KiB of ids and work lists (for any max_adapters).
+// What one call needs at the limits (128 tokens, H = 8192, any number of adapters): the fp32
+// LoRA delta, 128 x 8192 x 4 B = 4 MiB; the base GEMM's split-K partial sums, 3 tiles of
+// 128 tokens x 8192 features x 4 B = 12 MiB; and under 8 KiB of token ids, segments and work
+// units.  The array has 17 MiB; the assertion below recomputes the layout at the limits.
 constexpr size_t kScratchBytes = (size_t)LORA_NOALLOC_SCRATCH_BYTES;
+static_assert(segments_layout(kNoAllocMaxTokens, kNoAllocMaxH, LORA_MAX_ADAPTERS, 1).total <= kScratchBytes,
+              "the static scratch array must hold a workspace at the entry point's limits");
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 

@@ -826,27 +826,8 @@ int lora_status(lora_pool* p, lora_stream_t stream) {
 
 // ---- segment workspace -----------------------------------------------------------------
 namespace {
-struct SegLayout {
-  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials, total;
-  int32_t max_seg, unit_cap;
-};
 SegLayout seg_layout(const lora_pool* p, int32_t T_max, int32_t max_group) {
-  SegLayout L{};
-  L.max_seg = std::min<int32_t>(T_max, p->max_adapters);
-  L.unit_cap = T_max / kUnitTokens + L.max_seg + 1;
-  size_t off = 0;
-  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  L.perm = take((size_t)T_max * 4);
-  L.seg_off = take((size_t)(L.max_seg + 2) * 4);
-  L.seg_adapter = take((size_t)(L.max_seg + 1) * 4);
-  L.n_seg = take(16);
-  L.tok_adapter = take((size_t)T_max * 4);
-  L.units = take((size_t)L.unit_cap * 16);
-  L.n_units = take(16);
-  L.delta = take((size_t)max_group * T_max * p->H * 4);
-  L.partials = take((size_t)max_group * gemm_partial_floats(T_max, p->H) * 4);
-  L.total = off;
-  return L;
+  return segments_layout(T_max, p->H, p->max_adapters, max_group);
 }
 }  // namespace
 

@@ -177,13 +177,10 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
 int launch_segments_build(const lora_pool* p, const int32_t* token_adapter, int32_t T, const lora_segments* seg,
                           cudaStream_t st, bool pdl) {
   const size_t smem = 2 * (size_t)(p->max_adapters + 1) * sizeof(int32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(2 * (LORA_MAX_ADAPTERS + 1) * sizeof(int32_t)));
-    if (e != cudaSuccess) return lora_cuda_fail(e, "segments_kernel attribute");
-    attr_set = true;
-  }
+  static DeviceFlags attr;
+  int rc = ensure_smem_attr(attr, segments_kernel, (int)(2 * (LORA_MAX_ADAPTERS + 1) * sizeof(int32_t)),
+                            "segments_kernel attribute");
+  if (rc != LORA_OK) return rc;
   cudaError_t e = launch_pdl(pdl, segments_kernel, dim3(1), dim3(kThreads), smem, st, token_adapter, T,
                              (const int32_t*)p->d_rank, p->max_adapters, *seg, p->d_err);
   if (e == cudaSuccess) e = cudaGetLastError();

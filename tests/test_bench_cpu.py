@@ -94,5 +94,21 @@ def test_reference_arm_tiny_workload(capsys):
 def test_reference_arm_nonzero_rank_is_silent(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    bench.main(["--impl", "reference", "--config", "1", "--steps", "1"])
+    bench.main(["--impl", "reference", "--config", "1", "--steps", "1", "--gpus", "2"])
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_gpus_flag_relaunches_or_checks_the_world(monkeypatch):
+    """--gpus N outside torchrun starts N ranks; inside torchrun it must match WORLD_SIZE."""
+    calls = []
+    monkeypatch.setattr(bench, "relaunch_under_torchrun", lambda n, argv: calls.append((n, list(argv))) or 0)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    assert bench.check_world(1, ["--gpus", "1"]) is None and calls == []
+    assert bench.check_world(4, ["--gpus", "4", "--steps", "3"]) == 0
+    assert calls == [(4, ["--gpus", "4", "--steps", "3"])]
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    assert bench.check_world(4, []) is None
+    with pytest.raises(SystemExit):
+        bench.check_world(2, [])
+    with pytest.raises(SystemExit):
+        bench.check_world(0, [])

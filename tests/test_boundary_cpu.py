@@ -396,3 +396,22 @@ def test_packing_a_large_adapter_across_threads(L):
         assert np.array_equal(rows, want)
     finally:
         L.lora_pool_destroy(pool)
+
+
+def test_noalloc_scratch_holds_a_workspace_at_its_limits(L):
+    """The allocation-free entry point carves an ordinary segment workspace out of its static
+    array: at its token and hidden-size limits, with the largest adapter table, the workspace
+    must fit (the constants here are the header's)."""
+    hdr = open(os.path.join(ROOT, "include", "lora.h")).read()
+    consts = {k: int(eval(v)) for k, v in re.findall(r"#define (LORA_NOALLOC_\w+)\s+(\([^)]*\)|\d+)", hdr)}
+    assert consts == {"LORA_NOALLOC_MAX_TOKENS": L.LORA_NOALLOC_MAX_TOKENS, "LORA_NOALLOC_MAX_H": L.LORA_NOALLOC_MAX_H,
+                      "LORA_NOALLOC_SCRATCH_BYTES": L.LORA_NOALLOC_SCRATCH_BYTES}
+    pool = L.lora_pool_create(None, 1 << 20, L.LORA_NOALLOC_MAX_H, 4, L.LORA_MAX_ADAPTERS)
+    try:
+        need = L.lora_segments_size(pool, L.LORA_NOALLOC_MAX_TOKENS)
+        H, T = L.LORA_NOALLOC_MAX_H, L.LORA_NOALLOC_MAX_TOKENS
+        # fp32 delta (T x H) and split-K partial sums (3 tiles of T columns) dominate
+        assert need >= 4 * T * H + 3 * 4 * T * H
+        assert need <= L.LORA_NOALLOC_SCRATCH_BYTES
+    finally:
+        L.lora_pool_destroy(pool)

@@ -102,7 +102,7 @@ SMALL = [
     (2048, 256, [64, 8, 16, 32, 1], 1, 0.2),     # base GEMM splits K over a cluster of 4
     (1216, 64, [16, 64, 3], 2, 0.3),            # uneven 2-way K split, ragged last feature tile
     (2048, 2600, [16, 64, 8, 32], 1, 0.2),      # persistent GEMM, 176 tiles, ragged last token tile
-    (1024, 9700, [8, 16, 64], 1, 0.1),          # persistent GEMM with W multicast over 2 token tiles
+    (1024, 9700, [8, 16, 64], 1, 0.1),          # persistent GEMM, 304 tiles over two waves
 ]
 
 

@@ -59,6 +59,34 @@ def test_noalloc_matches_workspace_path_two_calls(L):
     sc.close()
 
 
+def test_noalloc_at_its_size_limits(L):
+    """128 tokens at H = 8192, the largest call the static array is sized for, twice in a row."""
+    import torch
+    H, T = L.LORA_NOALLOC_MAX_H, L.LORA_NOALLOC_MAX_TOKENS
+    wl = workloads.small(H=H, T=T, n_adapters=3, ranks=[64, 8, 33], seed=406, n_slots=1, none_share=0.1)
+    sc = DeviceScene(L, wl)
+    x = bits_to_torch(wl.x(0))
+    W = bits_to_torch(wl.W(0))
+    sc.segments(wl.token_adapter)
+    y_ref, _ = sc.forward(0, x, W, with_delta=False)
+    ta_dev = torch.from_numpy(np.asarray(wl.token_adapter, dtype=np.int32)).cuda()
+    ys = []
+    for _ in range(2):
+        y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        L.lora_linear_forward_noalloc(sc.pool, ta_dev, T, 0, x, W, y)
+        ys.append(y)
+    torch.cuda.synchronize()
+    b = _bf16(y_ref)
+    for y in ys:
+        a = _bf16(y)
+        assert np.all(np.abs(a - b) <= 1e-2 * (1 + np.abs(b)))
+    tokens = np.arange(0, T, 7)
+    y_or, _ = sc.oracle(wl.token_adapter, 0, wl.x(0), wl.W(0), tokens=tokens)
+    check_close(torch_to_bits(ys[1])[tokens], None, y_or, None, "noalloc at the limits")
+    L.lora_status(sc.pool)
+    sc.close()
+
+
 def test_noalloc_rejects_sizes_beyond_its_limit(L):
     import torch
     wl = workloads.small(H=256, T=4, n_adapters=1, ranks=[4], seed=405)
