@@ -500,21 +500,31 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 }
 
 // ---- persistent variant (batches of more than 256 tokens) ---------------------------------
-// Each CTA walks the tiles c, c + gridDim.x, ... (consecutive tiles: consecutive feature tiles of
-// one token tile, so the CTAs of a wave share x tiles in L2, and W stays in L2 across waves).
-// TMEM holds two accumulators of BN columns.  Warp 0 issues
-// TMA loads without pause across tile boundaries, warp 1 issues the MMAs of tile i into
+// One launch serves the n (1 .. LORA_MAX_GROUP) slots of a call that read the same x (q, k and v
+// of a layer, or a single slot).  Its tiles are (slot, token tile, feature tile) triples, slot
+// major; each CTA walks the tiles c, c + gridDim.x, ...  Consecutive tiles are consecutive
+// feature tiles of one token tile, so the CTAs of a wave share x tiles in L2, and a slot's W
+// stays in L2 while its tiles are in flight.  TMEM holds two accumulators of BN columns.  Warp 0
+// issues TMA loads without pause across tile boundaries, warp 1 issues the MMAs of tile i into
 // accumulator i % 2, and warps 4-7 (one per TMEM lane quarter) drain accumulator (i-1) % 2
 // meanwhile: add the delta (read straight from global memory), round to bf16, store y from
-// registers.  So a tile's epilogue runs under the next tile's main loop.
+// registers.  So a tile's epilogue runs under the next tile's main loop, and one launch for a
+// group pays the pipeline fill and the last, unhidden epilogue once instead of once per slot.
+// Every tile is computed by the same instruction sequence whichever CTA takes it, so each
+// slot's y is bitwise the y of a single-slot launch.
 struct PersistParams {
-  int32_t m_tiles, t_tiles;        // feature tiles; token tiles
-  int32_t n_ctiles;                // m_tiles * t_tiles
+  int32_t m_tiles, t_tiles;        // feature tiles; token tiles (per slot)
+  int32_t n_ctiles;                // n_group * m_tiles * t_tiles
+  int32_t n_group;
+  uint16_t* y[LORA_MAX_GROUP];
+  const float* delta[LORA_MAX_GROUP];
+  int32_t slot[LORA_MAX_GROUP];
 };
 
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, GemmParams p,
-                     PersistParams pp) {
+gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                     const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_w3,
+                     const __grid_constant__ CUtensorMap tm_x, GemmParams p, PersistParams pp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
@@ -531,6 +541,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
   const int nk = p.n_kb / kc;
   const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
   const int n_ctas = (int)gridDim.x;
+  const int per_slot = pp.m_tiles * pp.t_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
@@ -542,7 +553,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
       mbar_init(bar_tempty + 8 * b, 4);                 // one arrival per epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
   }
   if (warp == 1) {
@@ -561,8 +572,10 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
       uint32_t it = 0;
       bool ok = true;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
-        const int m0 = (ct % pp.m_tiles) * BM;
-        const int t0 = (ct / pp.m_tiles) * p.BN;
+        const int g = ct / per_slot, r = ct % per_slot;
+        const int m0 = (r % pp.m_tiles) * BM;
+        const int t0 = (r / pp.m_tiles) * p.BN;
+        const CUtensorMap* tw = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
         for (int i = 0; i < nk; ++i, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1;
@@ -575,7 +588,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
           const uint32_t st = s_base + (uint32_t)s * stage_bytes;
           for (int c = 0; c < kc; ++c) {
             const int kx = (i * kc + c) * BK;
-            tma_load_2d(st + (uint32_t)c * A_BYTES, &tm_w, kx, m0, bar_full + 8 * s, pol_w);
+            tma_load_2d(st + (uint32_t)c * A_BYTES, tw, kx, m0, bar_full + 8 * s, pol_w);
             tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
           }
         }
@@ -627,9 +640,20 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
     int tile = 0;
     for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas, ++tile) {
       const int b = tile & 1;
-      const int m0 = (ct % pp.m_tiles) * BM;
-      const int t0 = (ct / pp.m_tiles) * p.BN;
+      const int g = ct / per_slot, r = ct % per_slot;
+      const int m0 = (r % pp.m_tiles) * BM;
+      const int t0 = (r / pp.m_tiles) * p.BN;
       const int feat = m0 + row;
+      int slot = pp.slot[0];
+      uint16_t* y = pp.y[0];
+      const float* delta = pp.delta[0];
+#pragma unroll
+      for (int k = 1; k < LORA_MAX_GROUP; ++k)
+        if (g == k) {
+          slot = pp.slot[k];
+          y = pp.y[k];
+          delta = pp.delta[k];
+        }
       bool ok = mbar_wait(bar_tfull + 8 * b, (tile >> 1) & 1);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -641,7 +665,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
       const int n_chunks = p.BN / 32;
       for (int c4 = 0; c4 < n_chunks; c4 += 4) {
         unsigned pm[4];
-        presence_masks(p, p.slot, t0, c4, 1, n_chunks, lane, pm);
+        presence_masks(p, slot, t0, c4, 1, n_chunks, lane, pm);
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int c = c4 + k;
@@ -658,11 +682,11 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w, const __grid_cons
             float dv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              dv[i] = ((pmask >> i) & 1u) ? __ldg(p.delta + (size_t)(tc + i) * p.H + feat) : 0.f;
+              dv[i] = ((pmask >> i) & 1u) ? __ldg(delta + (size_t)(tc + i) * p.H + feat) : 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float a = __uint_as_float(v[i]);
-              if (tc + i < p.T) p.y[(size_t)(tc + i) * p.H + feat] = f32_to_bf16_rn((pmask >> i) & 1u ? a + dv[i] : a);
+              if (tc + i < p.T) y[(size_t)(tc + i) * p.H + feat] = f32_to_bf16_rn((pmask >> i) & 1u ? a + dv[i] : a);
             }
           }
         }
@@ -1021,63 +1045,52 @@ int persistent_ctas() {
 }
 }  // namespace
 
-int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
-  static DeviceFlags attr_single, attr_persist;
-  int rc0 = ensure_smem_attr(attr_single, gemm_lora_kernel, SMEM_BYTES, "gemm kernel attribute");
-  if (rc0 == LORA_OK) rc0 = ensure_smem_attr(attr_persist, gemm_lora_persistent, SMEM_BYTES, "gemm kernel attribute");
-  if (rc0 != LORA_OK) return rc0;
+namespace {
+// Tile geometry of one slot's base GEMM, as launch_gemm and the group launch choose it.
+struct Geometry {
+  int m_tiles, n_kb, ks, bn, n_tiles, kc, stages;
+};
+Geometry gemm_geometry(int T, int H, const GemmLaunch& G) {
+  Geometry g;
   const int n_sm = device_sm_count();
-  const int m_tiles = (G.H + BM - 1) / BM;
-  const int n_kb = G.H / BK;
-  int n_tiles, bn, ks = 1;
-  const int ks_try = n_kb % 4 == 0 ? 4 : 2;
-  const int bn_try = ((G.T + 32 * ks_try - 1) / (32 * ks_try)) * (32 * ks_try);
-  if (G.T <= MAX_BN && n_kb % 2 == 0 && G.partials &&
-      (int64_t)(ks_try - 1) * bn_try * m_tiles * BM <= G.partials_floats) {
+  g.m_tiles = (H + BM - 1) / BM;
+  g.n_kb = H / BK;
+  g.ks = 1;
+  const int ks_try = g.n_kb % 4 == 0 ? 4 : 2;
+  const int bn_try = ((T + 32 * ks_try - 1) / (32 * ks_try)) * (32 * ks_try);
+  if (T <= MAX_BN && g.n_kb % 2 == 0 && G.partials &&
+      (int64_t)(ks_try - 1) * bn_try * g.m_tiles * BM <= G.partials_floats) {
     // One token tile holds the whole batch (decode): K is split over a cluster of 4 (or 2) CTAs
     // per feature tile instead of cutting the tokens into narrow tiles, so each CTA streams
     // a quarter of W's K range plus the matching quarter of x, and the partial sums meet in
     // the scratch (L2).
-    ks = ks_try;
-    bn = bn_try;
-    n_tiles = 1;
+    g.ks = ks_try;
+    g.bn = bn_try;
+    g.n_tiles = 1;
   } else {
     // Token tiles: as few as possible (<= 256 tokens each), but enough to fill about 3/4 of the
     // SMs when the feature tiles alone do not, down to 32-token tiles.
-    n_tiles = (G.T + MAX_BN - 1) / MAX_BN;
-    const int want = (3 * n_sm / 4 + m_tiles - 1) / m_tiles;
-    const int max_tiles = (G.T + 31) / 32;
-    if (n_tiles < want) n_tiles = want < max_tiles ? want : max_tiles;
-    bn = (G.T + n_tiles - 1) / n_tiles;
-    bn = ((bn + 31) / 32) * 32;
-    if (bn > MAX_BN) bn = MAX_BN;
-    n_tiles = (G.T + bn - 1) / bn;
+    g.n_tiles = (T + MAX_BN - 1) / MAX_BN;
+    const int want = (3 * n_sm / 4 + g.m_tiles - 1) / g.m_tiles;
+    const int max_tiles = (T + 31) / 32;
+    if (g.n_tiles < want) g.n_tiles = want < max_tiles ? want : max_tiles;
+    g.bn = (T + g.n_tiles - 1) / g.n_tiles;
+    g.bn = ((g.bn + 31) / 32) * 32;
+    if (g.bn > MAX_BN) g.bn = MAX_BN;
+    g.n_tiles = (T + g.bn - 1) / g.bn;
   }
   // Each pipeline stage costs a fixed handshake on top of its data, and a CTA's TMA fill rate is
   // bounded, so stages are made large: up to 4 K chunks of 64, at most 96 KB (>= 2 stages).
-  const int kb_cta = n_kb / ks;
-  const int chunk_bytes = A_BYTES + bn * BK * 2;
-  int kc = 1;                       // wide tiles are MMA-bound: one chunk per stage
-  while (bn < 128 && kc < 4 && 2 * kc * chunk_bytes <= 96 * 1024 && kb_cta % (2 * kc) == 0) kc *= 2;
-  const int stage_bytes = kc * chunk_bytes;
-  int stages = STAGE_AREA / stage_bytes;
-  if (stages > MAX_STAGES) stages = MAX_STAGES;
-  const int ep_rows = bn / ks;      // token rows of the delta and y tiles one CTA's epilogue moves
-  // More tiles than resident CTAs: persistent CTAs overlap each tile's epilogue with the next
-  // tile's main loop.
-  const int n_ctiles = m_tiles * n_tiles;
-  const int n_res = ks == 1 ? persistent_ctas() : 0;
-  const bool persistent = ks == 1 && n_ctiles > n_res;
-  CUtensorMap tm_w, tm_x, tm_d, tm_y;
-  int rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)BM);
-  if (rc != LORA_OK) return rc;
-  rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)bn);
-  if (rc != LORA_OK) return rc;
-  // The delta tile the epilogue adds and the output tile it writes: [bn tokens][128 features].
-  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
-  if (rc != LORA_OK) return rc;
-  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
-  if (rc != LORA_OK) return rc;
+  const int kb_cta = g.n_kb / g.ks;
+  const int chunk_bytes = A_BYTES + g.bn * BK * 2;
+  g.kc = 1;                         // wide tiles are MMA-bound: one chunk per stage
+  while (g.bn < 128 && g.kc < 4 && 2 * g.kc * chunk_bytes <= 96 * 1024 && kb_cta % (2 * g.kc) == 0) g.kc *= 2;
+  g.stages = STAGE_AREA / (g.kc * chunk_bytes);
+  if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
+  return g;
+}
+
+GemmParams gemm_params(const GemmLaunch& G, const Geometry& g) {
   GemmParams P;
   P.y = G.y;
   P.delta = G.delta;
@@ -1087,38 +1100,84 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   P.err = G.err;
   P.T = G.T;
   P.H = G.H;
-  P.BN = bn;
-  P.n_kb = n_kb;
-  P.kc = kc;
-  P.stages = stages;
-  P.ks = ks;
+  P.BN = g.bn;
+  P.n_kb = g.n_kb;
+  P.kc = g.kc;
+  P.stages = g.stages;
+  P.ks = g.ks;
   P.slot = G.slot;
   P.n_slots = G.n_slots;
-  if (persistent) {
-    PersistParams pp;
-    pp.m_tiles = m_tiles;
-    pp.t_tiles = n_tiles;
-    pp.n_ctiles = n_ctiles;
-    cudaError_t e = launch_pdl(G.pdl, gemm_lora_persistent, dim3(n_res), dim3(THREADS), SMEM_BYTES, st, tm_w, tm_x,
-                               P, pp);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
+  return P;
+}
+
+// One persistent launch over the tiles of the n slots G[0..n) (same x, T and H).
+int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_t st) {
+  static DeviceFlags attr;
+  int rc = ensure_smem_attr(attr, gemm_lora_persistent, SMEM_BYTES, "gemm kernel attribute");
+  if (rc != LORA_OK) return rc;
+  const int H = G[0].H, T = G[0].T;
+  CUtensorMap tm_w[LORA_MAX_GROUP], tm_x;
+  for (int i = 0; i < n; ++i) {
+    rc = encode_2d(&tm_w[i], G[i].W, (uint64_t)H, (uint64_t)H, (uint32_t)BM);
+    if (rc != LORA_OK) return rc;
   }
+  for (int i = n; i < LORA_MAX_GROUP; ++i) tm_w[i] = tm_w[0];
+  rc = encode_2d(&tm_x, G[0].x, (uint64_t)H, (uint64_t)T, (uint32_t)g.bn);
+  if (rc != LORA_OK) return rc;
+  PersistParams pp = {};
+  pp.m_tiles = g.m_tiles;
+  pp.t_tiles = g.n_tiles;
+  pp.n_group = n;
+  pp.n_ctiles = n * g.m_tiles * g.n_tiles;
+  for (int i = 0; i < LORA_MAX_GROUP; ++i) {
+    const int j = i < n ? i : 0;
+    pp.y[i] = G[j].y;
+    pp.delta[i] = G[j].delta;
+    pp.slot[i] = G[j].slot;
+  }
+  int ctas = persistent_ctas();
+  if (ctas > pp.n_ctiles) ctas = pp.n_ctiles;
+  cudaError_t e = launch_pdl(G[0].pdl, gemm_lora_persistent, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
+                             tm_w[1], tm_w[2], tm_w[3], tm_x, gemm_params(G[0], g), pp);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
+}
+}  // namespace
+
+int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
+  const Geometry g = gemm_geometry(G.T, G.H, G);
+  // More tiles than resident CTAs: persistent CTAs overlap each tile's epilogue with the next
+  // tile's main loop.
+  if (g.ks == 1 && g.m_tiles * g.n_tiles > persistent_ctas()) return launch_persistent(&G, 1, g, st);
+  static DeviceFlags attr;
+  int rc = ensure_smem_attr(attr, gemm_lora_kernel, SMEM_BYTES, "gemm kernel attribute");
+  if (rc != LORA_OK) return rc;
+  const int ep_rows = g.bn / g.ks;  // token rows of the delta and y tiles one CTA's epilogue moves
+  CUtensorMap tm_w, tm_x, tm_d, tm_y;
+  rc = encode_2d(&tm_w, G.W, (uint64_t)G.H, (uint64_t)G.H, (uint32_t)BM);
+  if (rc != LORA_OK) return rc;
+  rc = encode_2d(&tm_x, G.x, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)g.bn);
+  if (rc != LORA_OK) return rc;
+  // The delta tile the epilogue adds and the output tile it writes: [bn tokens][128 features].
+  rc = encode_2d_plain(&tm_d, G.delta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
+  if (rc != LORA_OK) return rc;
+  rc = encode_2d_plain(&tm_y, G.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)G.H, (uint64_t)G.T, (uint32_t)ep_rows);
+  if (rc != LORA_OK) return rc;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ks, m_tiles, n_tiles);
+  cfg.gridDim = dim3(g.ks, g.m_tiles, g.n_tiles);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = ks;
+  attrs[0].val.clusterDim.x = g.ks;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = G.pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, gemm_params(G, g));
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_kernel launch");
 }
@@ -1231,19 +1290,31 @@ int launch_group_ks(const GemmLaunch* G, int n, const SplitK& sk, cudaStream_t s
 }
 }  // namespace
 
-bool gemm_group_fits(const GemmLaunch* G, int n) {
-  if (n < 2 || n > LORA_MAX_GROUP) return false;
-  SplitK sk;
-  if (!split_k_geometry(G[0].T, G[0].H, sk)) return false;
+namespace {
+bool same_input(const GemmLaunch* G, int n) {
   for (int i = 1; i < n; ++i)
     if (G[i].x != G[0].x || G[i].T != G[0].T || G[i].H != G[0].H || G[i].partials != G[0].partials) return false;
+  return true;
+}
+// The group's split-K launch (batches of <= 256 tokens): geometry and scratch for n slots.
+bool group_split_fits(const GemmLaunch* G, int n, SplitK& sk) {
+  if (!split_k_geometry(G[0].T, G[0].H, sk)) return false;
   const int m_tiles = (G[0].H + BM - 1) / BM;
   return G[0].partials && (int64_t)n * (sk.ks - 1) * sk.bn * m_tiles * BM <= G[0].partials_floats;
 }
+}  // namespace
+
+bool gemm_group_fits(const GemmLaunch* G, int n) {
+  if (n < 2 || n > LORA_MAX_GROUP || !same_input(G, n)) return false;
+  SplitK sk;
+  if (group_split_fits(G, n, sk)) return true;
+  return gemm_geometry(G[0].T, G[0].H, G[0]).ks == 1;     // larger batches: one persistent launch
+}
 
 int launch_gemm_group(const GemmLaunch* G, int n, cudaStream_t st) {
+  if (!gemm_group_fits(G, n)) return lora_fail(LORA_EINVAL, "launch_gemm_group: the slots do not form a group");
   SplitK sk;
-  if (!gemm_group_fits(G, n) || !split_k_geometry(G[0].T, G[0].H, sk))
-    return lora_fail(LORA_EINVAL, "launch_gemm_group: the group does not fit the split-K kernel");
-  return sk.ks == 4 ? launch_group_ks<4>(G, n, sk, st) : launch_group_ks<2>(G, n, sk, st);
+  if (group_split_fits(G, n, sk))
+    return sk.ks == 4 ? launch_group_ks<4>(G, n, sk, st) : launch_group_ks<2>(G, n, sk, st);
+  return launch_persistent(G, n, gemm_geometry(G[0].T, G[0].H, G[0]), st);
 }

@@ -162,15 +162,9 @@ def committed_traffic(kernel_file, config_key):
 # ------------------------------------------------------------------------------- workload bytes / flops
 def gemm_launch_groups(wl):
     """The slots each base-GEMM launch of a step covers (the library's rule, restated): a group
-    call on a batch of <= 256 tokens whose K splits evenly runs one grouped launch; otherwise
-    every slot has its own launch."""
-    out = []
-    for g in wl.slot_groups():
-        if len(g) > 1 and wl.T <= 256 and (wl.H // 64) % 2 == 0:
-            out.append(g)
-        else:
-            out += [[s] for s in g]
-    return out
+    call runs one grouped launch (split-K for batches of <= 256 tokens, persistent otherwise); a
+    single slot has its own launch."""
+    return [list(g) for g in wl.slot_groups()]
 
 
 def algorithmic(wl):
@@ -205,8 +199,11 @@ def gemm_kernel_names(wl, n_sm):
     """The base-GEMM kernels of a step, one name per distinct kernel ("a + b")."""
     names = []
     for g in gemm_launch_groups(wl):
-        k = (f"gemm_lora_group_splitk<{4 if (wl.H // 64) % 4 == 0 else 2}>" if len(g) > 1
-             else gemm_kernel_name(wl.H, wl.T, n_sm))
+        split = wl.T <= 256 and (wl.H // 64) % 2 == 0
+        if len(g) > 1:
+            k = f"gemm_lora_group_splitk<{4 if (wl.H // 64) % 4 == 0 else 2}>" if split else "gemm_lora_persistent"
+        else:
+            k = gemm_kernel_name(wl.H, wl.T, n_sm)
         if k not in names:
             names.append(k)
     return " + ".join(names)

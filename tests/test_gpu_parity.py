@@ -130,6 +130,9 @@ GROUP = [
     (384, 700, [8, 40, 64, 17], 3, 0.25, [1, 2]),            # several units per adapter
     (384, 100, [8, 64, 5], 3, 0.3, [0, 2, 1]),               # K split over 2 CTAs (6 blocks of 64)
     (4096, 200, [64, 32, 16, 8, 64, 16], 4, 0.1, [0, 1, 2]),  # 96 tiles: several per cluster
+    (1024, 2600, [16, 64, 8, 33], 3, 0.2, [0, 1, 2]),         # persistent group vs single-tile launches
+    (512, 700, [8, 64, 24], 2, 0.25, [1, 0]),                 # persistent group, 32-token tiles, 4 K chunks a stage
+    (192, 100, [8, 16, 64], 3, 0.2, [2, 0, 1]),               # K of 3 blocks: no split, persistent group
 ]
 
 
@@ -138,7 +141,7 @@ def test_group_forward_bitwise_equals_single_slot_calls(L, H, T, ranks, n_slots,
     """Slots that share x in one lora_linear_forward_group call give bit for bit what one
     lora_linear_forward call per slot gives, and both meet the oracle's tolerance.  Batches of
     <= 256 tokens take the grouped persistent split-K GEMM there and the single-slot split-K
-    GEMM here."""
+    GEMM here; larger batches one persistent launch over every slot's tiles there."""
     wl = workloads.small(H=H, T=T, n_adapters=len(ranks), ranks=ranks, seed=7 * H + T, n_slots=n_slots,
                          none_share=none_share)
     present = (lambda a: [True] * (n_slots - 1) + [a % 2 == 0]) if n_slots > 1 else None
