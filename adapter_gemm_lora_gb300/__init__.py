@@ -50,7 +50,7 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_adapter_ensure", "lora_pool_set_eviction", "lora_adapter_packed_size", "lora_adapter_pack",
             "lora_adapter_load_packed", "lora_adapter_wait", "lora_kv_grow", "lora_kv_free", "lora_kv_length",
             "lora_kv_table"]
-KINDS = ("segments", "delta", "gemm", "scatter")
+KINDS = ("segments", "delta", "gemm", "scatter", "shrink")
 
 
 class LoraError(RuntimeError):
@@ -65,7 +65,10 @@ class lora_segments(ctypes.Structure):
                 ("perm", ctypes.c_void_p), ("seg_off", ctypes.c_void_p), ("seg_adapter", ctypes.c_void_p),
                 ("n_seg", ctypes.c_void_p), ("tok_adapter", ctypes.c_void_p), ("units", ctypes.c_void_p),
                 ("n_units", ctypes.c_void_p), ("unit_cap", ctypes.c_int32), ("delta_slots", ctypes.c_int32),
-                ("delta", ctypes.c_void_p), ("gemm_partials", ctypes.c_void_p)]
+                ("delta", ctypes.c_void_p), ("gemm_partials", ctypes.c_void_p),
+                ("n_tiles_max", ctypes.c_int32), ("tile_plan", ctypes.c_void_p), ("entries", ctypes.c_void_p),
+                ("n_entries", ctypes.c_void_p), ("units_rest", ctypes.c_void_p), ("n_units_rest", ctypes.c_void_p),
+                ("s_lora", ctypes.c_void_p), ("shrink_scratch", ctypes.c_void_p)]
 
 
 class lora_pool_stats_t(ctypes.Structure):

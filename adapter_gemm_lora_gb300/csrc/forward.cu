@@ -6,7 +6,16 @@
 //   1. LoRA delta: s = x A, then delta = s B, per run of tokens sharing an adapter (paged
 //      gathers, fused in one kernel; s stays on chip), for every slot of the call at once
 //   2. base GEMM x W^T on tcgen05, epilogue y = bf16_rne(acc + delta): one launch per slot, or
-//      for a group of slots and a batch of <= 256 tokens one persistent launch over all of them
+//      one launch for a group of slots
+// A prefill-shaped batch (more than 256 tokens, on the persistent GEMM) is cut into 256-token
+// tiles; the tiles with at most LORA_TILE_ADAPTERS adapters ("fused", planned by the segment
+// build) take their LoRA term inside the GEMM instead ("Kernels for a batch of mixed ranks": many
+// tokens share each adapter there, so the expand is a dense product per tile):
+//   1. LoRA delta for the tokens of the other tiles only
+//   2. shrink of the fused tiles on tcgen05: s = x A as bf16 hi + lo parts
+//   3. (delta_dbg only) the GEMM's LoRA extension alone, fp32 into delta_dbg for the fused tiles
+//   4. base GEMM whose accumulator of a fused tile also takes s B (B pages read through the
+//      page table), y = bf16_rne(acc) there; other tiles add the delta as above
 #include <cuda_runtime.h>
 
 #include <string>
@@ -48,6 +57,32 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  GemmLaunch G[LORA_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    G[i] = GemmLaunch{};
+    G[i].x = static_cast<const uint16_t*>(x);
+    G[i].W = static_cast<const uint16_t*>(W[i]);
+    G[i].y = static_cast<uint16_t*>(y[i]);
+    G[i].tok_adapter = seg->tok_adapter;
+    G[i].ptab = p->d_ptab;
+    G[i].T = T;
+    G[i].H = H;
+    G[i].slot = slots[i];
+    G[i].n_slots = p->n_slots;
+    G[i].partials = seg->gemm_partials;
+    G[i].partials_floats = gemm_partial_floats(seg->T_max, H) * cap;
+    G[i].err = p->d_err;
+    G[i].pdl = !p->prof_on;
+    if (seg->tile_plan != nullptr && T > kTileTokens) {
+      G[i].tile_plan = seg->tile_plan;
+      G[i].s_lora = seg->s_lora + (size_t)i * seg->T_max * kSCols;
+      G[i].pool = static_cast<const uint16_t*>(p->pool_dev);
+      G[i].num_pages = p->num_pages;
+      G[i].rank = p->d_rank;
+    }
+  }
+  const bool fused = gemm_fused_fits(G, n);
+
   LoraLaunch L = {};
   L.pool = static_cast<const uint16_t*>(p->pool_dev);
   L.num_pages = p->num_pages;
@@ -67,6 +102,9 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
   L.ptab = p->d_ptab;
   L.rank = p->d_rank;
   L.seg = seg;
+  L.units = fused ? seg->units_rest : seg->units;
+  L.n_units = fused ? seg->n_units_rest : seg->n_units;
+  L.tile_plan = fused ? seg->tile_plan : nullptr;
   L.x = static_cast<const uint16_t*>(x);
   L.err = p->d_err;
   L.pdl = !p->prof_on;
@@ -76,23 +114,42 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
     rc = launch_lora_delta(L, st);
   }
   if (rc != LORA_OK) return rc;
+  for (int i = 0; i < n; ++i) G[i].delta = L.delta[i];
 
-  GemmLaunch G[LORA_MAX_GROUP];
-  for (int i = 0; i < n; ++i) {
-    G[i].x = static_cast<const uint16_t*>(x);
-    G[i].W = static_cast<const uint16_t*>(W[i]);
-    G[i].y = static_cast<uint16_t*>(y[i]);
-    G[i].delta = L.delta[i];
-    G[i].tok_adapter = seg->tok_adapter;
-    G[i].ptab = p->d_ptab;
-    G[i].T = T;
-    G[i].H = H;
-    G[i].slot = slots[i];
-    G[i].n_slots = p->n_slots;
-    G[i].partials = seg->gemm_partials;
-    G[i].partials_floats = gemm_partial_floats(seg->T_max, H) * cap;
-    G[i].err = p->d_err;
-    G[i].pdl = !p->prof_on;
+  if (fused) {
+    ShrinkLaunch S = {};
+    S.pool = L.pool;
+    S.num_pages = p->num_pages;
+    S.H = H;
+    S.T = T;
+    S.n_slots = p->n_slots;
+    S.n_group = n;
+    for (int i = 0; i < n; ++i) S.slot[i] = slots[i];
+    S.ptab = p->d_ptab;
+    S.rank = p->d_rank;
+    S.seg = seg;
+    S.x = L.x;
+    S.err = p->d_err;
+    S.pdl = L.pdl;
+    {
+      ProfScope prof(p, LORA_KIND_SHRINK, st);
+      rc = launch_lora_shrink(S, st);
+    }
+    if (rc != LORA_OK) return rc;
+    if (delta_dbg != nullptr) {         // the fused tiles' LoRA term, as the GEMM computes it, alone
+      bool any = false;
+      for (int i = 0; i < n; ++i) {
+        G[i].lora_dbg = delta_dbg[i] ? delta_dbg[i] : seg->delta + (size_t)i * seg->T_max * H;
+        any = any || delta_dbg[i] != nullptr;
+      }
+      if (any) {
+        ProfScope prof(p, LORA_KIND_GEMM, st);
+        rc = launch_gemm_fused(G, n, true, st);
+        if (rc != LORA_OK) return rc;
+      }
+    }
+    ProfScope prof(p, LORA_KIND_GEMM, st);
+    return launch_gemm_fused(G, n, false, st);
   }
   if (gemm_group_fits(G, n)) {          // decode-sized batch: one launch for every slot of the group
     ProfScope prof(p, LORA_KIND_GEMM, st);

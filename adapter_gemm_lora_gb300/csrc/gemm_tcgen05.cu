@@ -25,14 +25,7 @@
 // (griddepcontrol.wait) only before its epilogue reads the delta.
 // Every mbarrier wait is bounded (~2 s of SM cycles); on expiry the CTA raises the device error word,
 // skips the rest of its work and frees TMEM before returning.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "lora_internal.h"
+#include "tc_ptx.h"
 
 namespace {
 
@@ -42,7 +35,7 @@ constexpr int MAX_BN = 256;      // tokens per tile (MMA N)
 constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int STAGE_AREA = 192 * 1024;        // ring of stages; reused by the epilogue
-constexpr int BAR_BYTES = 256;
+constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + STAGE_AREA + BAR_BYTES;
 constexpr int THREADS = 256;
 
@@ -56,169 +49,6 @@ struct GemmParams {
   int32_t T, H, BN, n_kb, kc, stages, ks, slot, n_slots;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
-  atomicCAS(err, 0, LORA_EDEVICE);
-  atomicOr(err + 1, bits);
-}
-
-// ---- mbarrier ---------------------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)   // suspend-time hint (ns); the phase completing wakes it
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase of the given parity to complete; false if the wait runs out.  The bound
-// is counted with the SM's own cycle counter (clock64): it is cheap to read, unlike the global
-// timer, whose read latency would otherwise land on every pipeline step.  4e9 cycles is about
-// 2 s at the maximum SM clock.
-constexpr long long kWaitLimitCycles = 4000000000ll;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long c0 = clock64();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - c0 > kWaitLimitCycles) return false;
-  }
-}
-
-// ---- TMA --------------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_plain(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// ---- clusters and programmatic dependent launch --------------------------------------------
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// ---- tcgen05 ----------------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on `bar` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// 32 lanes x 32 consecutive columns of 32-bit TMEM data: thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-// 32 lanes x 16 consecutive columns.
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor for a K-major operand tile written by TMA with the
-// 128-byte swizzle: rows of 64 bf16 (128 B), 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4)   // start address, 16-byte units
-         | ((uint64_t)1 << 16)                  // leading-dimension byte offset (unused here)
-         | ((uint64_t)(1024 >> 4) << 32)        // stride-dimension byte offset: 8 rows x 128 B
-         | ((uint64_t)1 << 46)                  // descriptor version for tcgen05
-         | ((uint64_t)2 << 61);                 // swizzle mode: 128-byte
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
-  return (1u << 4)                           // D format: f32
-         | (1u << 7)                         // A format: bf16
-         | (1u << 10)                        // B format: bf16
-         | ((uint32_t)(N >> 3) << 17)        // N / 8
-         | ((uint32_t)(M >> 4) << 24);       // M / 16
-}
-
-__host__ __device__ inline uint32_t tmem_cols_for(int bn) {
-  uint32_t c = 32;
-  while ((int)c < bn) c <<= 1;
-  return c;
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 // Ballot masks of the tokens (columns) that carry LoRA on this slot, for the 32-column chunks
 // c0, c0 + step, ... (at most 4): all id loads are issued before any page-table load, so the two
@@ -240,10 +70,6 @@ __device__ __forceinline__ void presence_masks(const GemmParams& p, int slot, in
   for (int k = 0; k < 4; ++k) pm[k] = __ballot_sync(0xffffffffu, present[k]);
 }
 
-__device__ __forceinline__ void bulk_commit_wait_read() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // Epilogue when K is split over a cluster of ks CTAs (one token tile of BN columns).  CTA `me`
 // owns token columns [me*w, (me+1)*w), w = BN/ks.  Every CTA writes the fp32 partial sums of
@@ -512,6 +338,20 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 // group pays the pipeline fill and the last, unhidden epilogue once instead of once per slot.
 // Every tile is computed by the same instruction sequence whichever CTA takes it, so each
 // slot's y is bitwise the y of a single-slot launch.
+//
+// Fused tiles (256-token tiles with at most LORA_TILE_ADAPTERS adapters, planned by the segment
+// build): the LoRA term is added inside the accumulator instead of from a delta buffer.  After
+// the K blocks of x W^T the tile gets, for each of its adapters b that has LoRA on the slot, the
+// K extension
+//     acc[n, t] += sum_j B_b[j, n] s_hi[t, j] + sum_j B_b[j, n] s_lo[t, j],    j < r_b rounded up to 16,
+// where s = s_hi + s_lo is x A_b for the tile's tokens of adapter b and zero for its other tokens
+// (written by the shrink kernel).  Each adapter takes two ring stages: the first holds its B page
+// rows for the tile's 128 features (gathered by warps 2-3 with 16-byte cp.async copies into the
+// MN-major 128-byte-swizzled layout, a page row's 64-feature half being one 128-byte atom row)
+// and the s_hi tile (TMA), the second the s_lo tile (TMA); the MMAs read B_b transposed (MN-major
+// A operand).  The epilogue of a fused tile adds no delta: y = bf16(acc), rounded once.  A
+// LoRA-only launch (for delta_dbg) runs the extension alone on the fused tiles and writes the
+// fp32 accumulator to the debug buffer.
 struct PersistParams {
   int32_t m_tiles, t_tiles;        // feature tiles; token tiles (per slot)
   int32_t n_ctiles;                // n_group * m_tiles * t_tiles
@@ -519,34 +359,90 @@ struct PersistParams {
   uint16_t* y[LORA_MAX_GROUP];
   const float* delta[LORA_MAX_GROUP];
   int32_t slot[LORA_MAX_GROUP];
+  // fused tiles (tile_plan == nullptr: none)
+  const int32_t* tile_plan;
+  const uint16_t* pool;
+  int64_t num_pages;
+  const int32_t* rank;
+  int32_t lora_only;               // 1: the LoRA extension alone, fp32 into dbg, fused tiles only
+  float* dbg[LORA_MAX_GROUP];
 };
+
+// The LoRA extension of one tile on one slot: -1 when the tile is not fused, else the number of
+// the tile's adapters that carry LoRA on the slot, with their page-table rows and ranks.
+struct TileLora {
+  int nb;
+  const int32_t* tab[kTileAdapters];
+  int r[kTileAdapters];
+  int tmap_b[kTileAdapters];        // the adapter's tile slot: its columns in s_lora
+};
+__device__ __forceinline__ void tile_lora(const PersistParams& pp, const GemmParams& p, int tile, int slot,
+                                          TileLora& L) {
+  L.nb = -1;
+  if (pp.tile_plan == nullptr) return;
+  const int32_t* pl = pp.tile_plan + (size_t)tile * kPlanStride;
+  const int n = __ldg(pl);
+  if (n < 0) return;
+  L.nb = 0;
+  for (int b = 0; b < n && b < kTileAdapters; ++b) {
+    const int a = __ldg(pl + 1 + b);
+    if (a < 0) continue;
+    const int r = __ldg(pp.rank + a);
+    const int32_t* tab = p.ptab + ((int64_t)a * p.n_slots + slot) * kTabStride;
+    if (r < 1 || r > LORA_MAX_RANK || __ldg(tab) < 0) continue;
+    L.tab[L.nb] = tab;
+    L.r[L.nb] = r;
+    L.tmap_b[L.nb] = b;
+    ++L.nb;
+  }
+}
+__device__ __forceinline__ int slot_of(const PersistParams& pp, int g) {
+  int slot = pp.slot[0];
+#pragma unroll
+  for (int k = 1; k < LORA_MAX_GROUP; ++k)
+    if (g == k) slot = pp.slot[k];
+  return slot;
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_w3,
-                     const __grid_constant__ CUtensorMap tm_x, GemmParams p, PersistParams pp) {
+                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_s0,
+                     const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_s2,
+                     const __grid_constant__ CUtensorMap tm_s3, GemmParams p, PersistParams pp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGE_AREA);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 4);
+  // full[MAX_STAGES], empty[MAX_STAGES], tfull[2], tempty[2], wl[MAX_STAGES], go[MAX_STAGES], then
+  // the TMEM address
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * MAX_STAGES + 4);
   const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * MAX_STAGES;
   const uint32_t bar_tfull = bar_full + 16 * MAX_STAGES, bar_tempty = bar_tfull + 16;
+  const uint32_t bar_wl = bar_tempty + 16;              // B page rows of a LoRA stage landed
+  // The producer, which waits on every stage's empty barrier in order, tells the loader warps that
+  // the ring slot of a LoRA stage is free.  (The loaders skip the base stages, so a parity wait of
+  // theirs on the empty barrier could be several phases behind and pass or block wrongly.)
+  const uint32_t bar_go = bar_wl + 8 * MAX_STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int stages = p.stages;
   const int kc = p.kc;
   const uint32_t xb = (uint32_t)(p.BN * BK * 2);
   const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
-  const int nk = p.n_kb / kc;
+  const int nk = pp.lora_only ? 0 : p.n_kb / kc;         // base stages per tile
   const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
   const int n_ctas = (int)gridDim.x;
   const int per_slot = pp.m_tiles * pp.t_tiles;
+  const bool fused_mode = pp.tile_plan != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_wl + 8 * s, 2);                     // one arrival per loader warp
+      mbar_init(bar_go + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
@@ -570,12 +466,14 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       const uint64_t pol_w = policy_evict_last();       // W tiles are re-read by other token tiles
       const uint64_t pol_x = policy_evict_last();       // x tiles are re-read by other feature tiles
       uint32_t it = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
         const int m0 = (r % pp.m_tiles) * BM;
-        const int t0 = (r / pp.m_tiles) * p.BN;
+        const int tt = r / pp.m_tiles;
+        const int t0 = tt * p.BN;
         const CUtensorMap* tw = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
+        const CUtensorMap* ts = g == 0 ? &tm_s0 : g == 1 ? &tm_s1 : g == 2 ? &tm_s2 : &tm_s3;
         for (int i = 0; i < nk; ++i, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1;
@@ -592,21 +490,56 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
             tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
           }
         }
+        if (!ok || !fused_mode) continue;
+        if (!waited) {                                  // the plan and s come from earlier kernels
+          grid_dependency_wait();
+          waited = true;
+        }
+        TileLora TL;
+        tile_lora(pp, p, tt, slot_of(pp, g), TL);
+        for (int b = 0; b < TL.nb && ok; ++b) {         // s_hi, then s_lo, of adapter b
+          for (int part = 0; part < 2; ++part, ++it) {
+            const int s = it % stages;
+            if (!mbar_wait(bar_empty + 8 * s, ((it / stages) & 1) ^ 1)) {
+              flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+              ok = false;
+              break;
+            }
+            if (part == 0) mbar_arrive(bar_go + 8 * s);     // the loaders may write this slot's B rows
+            mbar_arrive_expect_tx(bar_full + 8 * s, xb);
+            tma_load_2d(s_base + (uint32_t)s * stage_bytes + A_BYTES, ts,
+                        TL.tmap_b[b] * 2 * LORA_MAX_RANK + part * LORA_MAX_RANK, t0, bar_full + 8 * s, pol_x);
+          }
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {                                    // MMA issuer
       const uint32_t idesc = make_idesc_bf16(BM, p.BN);
-      uint32_t it = 0;
+      const uint32_t idesc_mn = idesc | kIdescAMnMajor;
+      uint32_t it = 0, wl_par = 0;
       int tile = 0;
-      bool ok = true;
-      for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas, ++tile) {
+      bool ok = true, waited = false;
+      for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
+        const int g = ct / per_slot, r = ct % per_slot;
+        const int tt = r / pp.m_tiles;
+        TileLora TL;
+        TL.nb = -1;
+        if (pp.lora_only) {
+          if (!waited) {
+            grid_dependency_wait();
+            waited = true;
+          }
+          tile_lora(pp, p, tt, slot_of(pp, g), TL);
+          if (TL.nb < 0) continue;                        // the LoRA-only pass skips unfused tiles
+        }
         const int b = tile & 1;
         if (!mbar_wait(bar_tempty + 8 * b, ((tile >> 1) & 1) ^ 1)) {   // accumulator b drained
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
         }
+        ++tile;
         tc_fence_after();
         const uint32_t acc = tmem + (uint32_t)b * acc_cols;
         for (int i = 0; i < nk; ++i, ++it) {
@@ -628,33 +561,129 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           }
           mma_commit(bar_empty + 8 * s);
         }
+        if (fused_mode && !pp.lora_only && ok) {         // the plan is read once the base K blocks are issued
+          if (!waited) {
+            grid_dependency_wait();
+            waited = true;
+          }
+          tile_lora(pp, p, tt, slot_of(pp, g), TL);
+        }
+        bool first = nk == 0;                             // LoRA-only: the first MMA starts the sum
+        for (int lb = 0; lb < TL.nb && ok; ++lb, it += 2) {
+          const int s0 = it % stages, s1 = (it + 1) % stages;
+          const uint32_t ph0 = (it / stages) & 1, ph1 = ((it + 1) / stages) & 1;
+          const uint32_t wph = (wl_par >> s0) & 1u;
+          wl_par ^= 1u << s0;
+          if (!mbar_wait(bar_full + 8 * s0, ph0) || !mbar_wait(bar_wl + 8 * s0, wph) ||
+              !mbar_wait(bar_full + 8 * s1, ph1)) {
+            flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st0 = s_base + (uint32_t)s0 * stage_bytes, st1 = s_base + (uint32_t)s1 * stage_bytes;
+          const uint64_t bh = sw128_kmajor_desc(st0 + A_BYTES), bl = sw128_kmajor_desc(st1 + A_BYTES);
+          const int n16 = (TL.r[lb] + 15) / 16;
+          for (int k = 0; k < n16; ++k) {                 // 16 rank columns: two 8-row groups of B
+            const uint64_t ad = sw128_mnmajor_desc(st0 + (uint32_t)k * 4096u, 1024u, 2048u);
+            mma_bf16_ss(acc, ad, bh + 2 * k, idesc_mn, first ? 0u : 1u);
+            first = false;
+            mma_bf16_ss(acc, ad, bl + 2 * k, idesc_mn, 1u);
+          }
+          mma_commit(bar_empty + 8 * s0);
+          mma_commit(bar_empty + 8 * s1);
+        }
         if (ok) mma_commit(bar_tfull + 8 * b);            // accumulator b complete
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    // ---- B page rows of the fused tiles' LoRA stages (64 threads) ----
+    if (fused_mode) {
+      const int l = threadIdx.x - 64;
+      grid_dependency_wait();
+      uint32_t it = 0, go_par = 0;
+      bool ok = true;
+      for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
+        const int g = ct / per_slot, r = ct % per_slot;
+        const int m0 = (r % pp.m_tiles) * BM;
+        const int tt = r / pp.m_tiles;
+        TileLora TL;
+        tile_lora(pp, p, tt, slot_of(pp, g), TL);
+        it += nk;
+        for (int lb = 0; lb < TL.nb && ok; ++lb, it += 2) {
+          // chunk c = l + 64 i: row j = c / 16 (rank column), 64-feature half h = (c / 8) % 2,
+          // 16-byte piece c % 8; page ids are read before the stage is free
+          const int r16 = (TL.r[lb] + 15) & ~15;
+          int64_t src[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = l + 64 * i;
+            const int j = c >> 4, h = (c >> 3) & 1, piece = c & 7;
+            const int f = m0 + h * 64 + piece * 8;
+            src[i] = -1;                                  // zero: past the rank, past H or a bad page
+            if (c < r16 * 16 && j < TL.r[lb] && f < p.H) {
+              const int64_t page = __ldg(TL.tab[lb] + LORA_MAX_RANK + j);
+              if (page >= 0 && page < pp.num_pages)
+                src[i] = page * p.H + f;
+              else
+                flag_error(p.err, LORA_DEV_BAD_PAGE);
+            }
+          }
+          const int s = it % stages;
+          const uint32_t gph = (go_par >> s) & 1u;
+          go_par ^= 1u << s;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_go + 8 * s, gph));
+          if (!ok) break;
+          const uint32_t st = s_base + (uint32_t)s * stage_bytes;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = l + 64 * i;
+            if (c < r16 * 16) {
+              const int j = c >> 4, h = (c >> 3) & 1, piece = c & 7;
+              cp_async_16(st + (uint32_t)(j >> 3) * 2048u + (uint32_t)h * 1024u + sw128_offset(j, piece),
+                          pp.pool + (src[i] >= 0 ? src[i] : 0), src[i] >= 0);
+            }
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_wl + 8 * s);
+        }
+      }
+      if (!ok && lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
+    }
+  } else {
     // ---- epilogue warps: TMEM lane quarter q = warp - 4 ----
     const int q = warp - 4;
     const int row = q * 32 + lane;
-    pdl_wait_then_release();                            // delta and ids come from earlier kernels
+    pdl_wait_then_release();                            // delta, ids and the plan come from earlier kernels
     int tile = 0;
-    for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas, ++tile) {
-      const int b = tile & 1;
+    for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas) {
       const int g = ct / per_slot, r = ct % per_slot;
       const int m0 = (r % pp.m_tiles) * BM;
       const int t0 = (r / pp.m_tiles) * p.BN;
       const int feat = m0 + row;
-      int slot = pp.slot[0];
+      const int slot = slot_of(pp, g);
+      TileLora TL;
+      TL.nb = -1;
+      if (fused_mode) tile_lora(pp, p, r / pp.m_tiles, slot, TL);
+      if (pp.lora_only && TL.nb < 0) continue;
+      const int b = tile & 1;
+      const uint32_t tph = (tile >> 1) & 1;
+      ++tile;
       uint16_t* y = pp.y[0];
       const float* delta = pp.delta[0];
+      float* dbg = pp.dbg[0];
 #pragma unroll
       for (int k = 1; k < LORA_MAX_GROUP; ++k)
         if (g == k) {
-          slot = pp.slot[k];
           y = pp.y[k];
           delta = pp.delta[k];
+          dbg = pp.dbg[k];
         }
-      bool ok = mbar_wait(bar_tfull + 8 * b, (tile >> 1) & 1);
+      bool ok = mbar_wait(bar_tfull + 8 * b, tph);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
@@ -664,8 +693,8 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       const uint32_t acc_row = tmem + (uint32_t)b * acc_cols + ((uint32_t)(q * 32) << 16);
       const int n_chunks = p.BN / 32;
       for (int c4 = 0; c4 < n_chunks; c4 += 4) {
-        unsigned pm[4];
-        presence_masks(p, slot, t0, c4, 1, n_chunks, lane, pm);
+        unsigned pm[4] = {0u, 0u, 0u, 0u};              // a fused tile's LoRA term is in the accumulator
+        if (TL.nb < 0) presence_masks(p, slot, t0, c4, 1, n_chunks, lane, pm);
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int c = c4 + k;
@@ -675,8 +704,13 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           uint32_t v[32];
           tmem_ld_32x32b_x32(acc_row + (uint32_t)(c * 32), v);
           tmem_ld_wait();
-          const unsigned pmask = k == 0 ? pm[0] : k == 1 ? pm[1] : k == 2 ? pm[2] : pm[3];
-          if (feat < p.H) {
+          if (feat < p.H && pp.lora_only) {
+            const bool any = TL.nb > 0;                 // no LoRA stage: the term is zero
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (tc + i < p.T) dbg[(size_t)(tc + i) * p.H + feat] = any ? __uint_as_float(v[i]) : 0.f;
+          } else if (feat < p.H) {
+            const unsigned pmask = k == 0 ? pm[0] : k == 1 ? pm[1] : k == 2 ? pm[2] : pm[3];
             // every load of the chunk before its first store (y may alias delta as far as the
             // compiler knows)
             float dv[32];
@@ -722,37 +756,6 @@ struct GroupParams {
   int32_t m_tiles;                 // feature tiles per slot
   int32_t n_tiles;                 // (slot, feature tile) pairs
 };
-
-// Arrive on the mbarrier at `local_bar`'s offset in CTA `rank` of the cluster, with cluster-scope
-// release: this thread's earlier writes, global memory included, are visible to any thread of
-// the cluster whose acquire wait observes the phase the arrival completes.
-__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t local_bar, uint32_t rank) {
-  uint32_t rb;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
-      : "memory");
-  return ok != 0;
-}
-// Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-  const long long c0 = clock64();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-    if (clock64() - c0 > kWaitLimitCycles) return false;
-  }
-}
 
 template <int KS>
 __global__ void __launch_bounds__(GROUP_THREADS, 1)
@@ -980,50 +983,6 @@ gemm_lora_group_splitk(const __grid_constant__ CUtensorMap tm_w0, const __grid_c
   cluster_sync_all();                             // no peer may still arrive on this CTA's barriers
 }
 
-// ---- host side --------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 2-D bf16 tensor [rows][inner] row-major, box = box_rows x 64 elements, 128-byte swizzle.
-int encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  auto fn = get_encode_fn();
-  if (!fn) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string((int)r));
-  return LORA_OK;
-}
-
-// 2-D tensor [rows][inner] row-major without swizzle, box = box_rows x 128 elements.
-int encode_2d_plain(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint32_t esize, uint64_t inner,
-                    uint64_t rows, uint32_t box_rows) {
-  auto fn = get_encode_fn();
-  if (!fn) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * esize};
-  const cuuint32_t box[2] = {(cuuint32_t)BM, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return lora_fail(LORA_ECUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string((int)r));
-  return LORA_OK;
-}
-
 }  // namespace
 
 namespace {
@@ -1110,8 +1069,10 @@ GemmParams gemm_params(const GemmLaunch& G, const Geometry& g) {
   return P;
 }
 
-// One persistent launch over the tiles of the n slots G[0..n) (same x, T and H).
-int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_t st) {
+// One persistent launch over the tiles of the n slots G[0..n) (same x, T and H); with `fused`, the
+// plan's fused tiles take their LoRA term in the GEMM (lora_only: that term alone, into lora_dbg).
+int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_t st, bool fused = false,
+                      bool lora_only = false) {
   static DeviceFlags attr;
   int rc = ensure_smem_attr(attr, gemm_lora_persistent, SMEM_BYTES, "gemm kernel attribute");
   if (rc != LORA_OK) return rc;
@@ -1124,6 +1085,15 @@ int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_
   for (int i = n; i < LORA_MAX_GROUP; ++i) tm_w[i] = tm_w[0];
   rc = encode_2d(&tm_x, G[0].x, (uint64_t)H, (uint64_t)T, (uint32_t)g.bn);
   if (rc != LORA_OK) return rc;
+  CUtensorMap tm_s[LORA_MAX_GROUP];
+  for (int i = 0; i < LORA_MAX_GROUP; ++i) {
+    if (fused && i < n) {
+      rc = encode_2d(&tm_s[i], G[i].s_lora, (uint64_t)kSCols, (uint64_t)T, (uint32_t)g.bn);
+      if (rc != LORA_OK) return rc;
+    } else {
+      tm_s[i] = tm_x;                                   // never read
+    }
+  }
   PersistParams pp = {};
   pp.m_tiles = g.m_tiles;
   pp.t_tiles = g.n_tiles;
@@ -1134,11 +1104,20 @@ int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_
     pp.y[i] = G[j].y;
     pp.delta[i] = G[j].delta;
     pp.slot[i] = G[j].slot;
+    pp.dbg[i] = G[j].lora_dbg;
+  }
+  if (fused) {
+    pp.tile_plan = G[0].tile_plan;
+    pp.pool = G[0].pool;
+    pp.num_pages = G[0].num_pages;
+    pp.rank = G[0].rank;
+    pp.lora_only = lora_only ? 1 : 0;
   }
   int ctas = persistent_ctas();
   if (ctas > pp.n_ctiles) ctas = pp.n_ctiles;
   cudaError_t e = launch_pdl(G[0].pdl, gemm_lora_persistent, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
-                             tm_w[1], tm_w[2], tm_w[3], tm_x, gemm_params(G[0], g), pp);
+                             tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3],
+                             gemm_params(G[0], g), pp);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
 }
@@ -1309,6 +1288,19 @@ bool gemm_group_fits(const GemmLaunch* G, int n) {
   SplitK sk;
   if (group_split_fits(G, n, sk)) return true;
   return gemm_geometry(G[0].T, G[0].H, G[0]).ks == 1;     // larger batches: one persistent launch
+}
+
+bool gemm_fused_fits(const GemmLaunch* G, int n) {
+  if (n < 1 || n > LORA_MAX_GROUP || !same_input(G, n) || !G[0].tile_plan || G[0].T <= kTileTokens) return false;
+  const Geometry g = gemm_geometry(G[0].T, G[0].H, G[0]);
+  if (g.ks != 1 || g.bn != kTileTokens || g.kc != 1 || g.n_kb < kShrinkCluster) return false;
+  // a single slot keeps the one-wave kernel when its tiles fit the GPU at once
+  return n > 1 || g.m_tiles * g.n_tiles > persistent_ctas();
+}
+
+int launch_gemm_fused(const GemmLaunch* G, int n, bool lora_only, cudaStream_t st) {
+  if (!gemm_fused_fits(G, n)) return lora_fail(LORA_EINVAL, "launch_gemm_fused: batch geometry without fused tiles");
+  return launch_persistent(G, n, gemm_geometry(G[0].T, G[0].H, G[0]), st, true, lora_only);
 }
 
 int launch_gemm_group(const GemmLaunch* G, int n, cudaStream_t st) {

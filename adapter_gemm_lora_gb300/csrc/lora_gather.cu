@@ -153,8 +153,8 @@ struct Unit {
   const int32_t* tab;      // the adapter's page table on the item's slot
   float* delta;            // the slot's delta rows
 };
-__device__ __forceinline__ int4 load_rec(const lora_segments& seg, int u, int n_units) {
-  return u < n_units ? __ldg(reinterpret_cast<const int4*>(seg.units) + u) : make_int4(0, 0, 0, 0);
+__device__ __forceinline__ int4 load_rec(const LoraLaunch& L, int u, int n_units) {
+  return u < n_units ? __ldg(reinterpret_cast<const int4*>(L.units) + u) : make_int4(0, 0, 0, 0);
 }
 // Item i of the launch is unit i / n_group on group member i % n_group.
 __device__ __forceinline__ Unit unit_of(const LoraLaunch& L, const int4& rec, int g) {
@@ -179,10 +179,11 @@ struct Gathered {
   int32_t tok[4];
 };
 // Issue this lane's loads for unit U (values are consumed one unit later).  ntok_lane: how many
-// perm entries each lane reads; entry k of lane l is token tok_index(l, k) of the unit.
+// perm entries each lane reads; entry k of lane l is token tok_index(l, k) of the unit.  A token
+// of a fused tile (its LoRA term comes from the GEMM) reads as -1, like a position past the unit.
 template <int NTOK, typename F>
-__device__ __forceinline__ void gather_issue(const lora_segments& seg, const Unit& U, int lane, F tok_index,
-                                             Gathered& G) {
+__device__ __forceinline__ void gather_issue(const LoraLaunch& L, const lora_segments& seg, const Unit& U, int lane,
+                                             F tok_index, Gathered& G) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int j = lane + 32 * h;
@@ -193,6 +194,11 @@ __device__ __forceinline__ void gather_issue(const lora_segments& seg, const Uni
   for (int k = 0; k < NTOK; ++k) {
     const int t = tok_index(lane, k);
     G.tok[k] = t < U.n_tok ? __ldg(seg.perm + U.t_begin + t) : -1;
+  }
+  if (L.tile_plan != nullptr) {
+#pragma unroll
+    for (int k = 0; k < NTOK; ++k)
+      if (G.tok[k] >= 0 && __ldg(L.tile_plan + (size_t)(G.tok[k] / kTileTokens) * kPlanStride) >= 0) G.tok[k] = -1;
   }
 }
 __device__ __forceinline__ bool page_ok(int32_t p, int64_t num_pages) { return p >= 0 && p < num_pages; }
@@ -250,7 +256,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   const int Hq = H / kCluster;                            // features per CTA (multiple of 16)
   const int n_fb = (Hq + kFB - 1) / kFB;
   const int f_cta = (int)q * Hq;
-  const int n_units = *seg.n_units;
+  const int n_units = *L.n_units;
   const int ng = L.n_group;
   const int n_items = n_units * ng;                       // item i: unit i / ng on member i % ng
   const int n_groups = gridDim.x / kCluster;
@@ -267,16 +273,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     auto tok_lane = [](int l, int) { return l; };
     uint32_t it = 0, xi = 0;                              // ring stages and x buffer fills issued
     bool ok = true;
-    int4 rec = load_rec(seg, item_at(0) / ng, n_units);
+    int4 rec = load_rec(L, item_at(0) / ng, n_units);
     Gathered G;
     Unit U = unit_of(L, rec, item_at(0) % ng);
-    gather_issue<1>(seg, U, lane, tok_lane, G);
-    int4 rec_next = load_rec(seg, item_at(1) / ng, n_units);
+    gather_issue<1>(L, seg, U, lane, tok_lane, G);
+    int4 rec_next = load_rec(L, item_at(1) / ng, n_units);
     for (int w = 0; item_at(w) < n_items && ok; ++w) {   // the producer alone may stop early
       const Unit Un = unit_of(L, rec_next, item_at(w + 1) % ng);
       Gathered Gn;
-      gather_issue<1>(seg, Un, lane, tok_lane, Gn);
-      rec_next = load_rec(seg, item_at(w + 2) / ng, n_units);
+      gather_issue<1>(L, seg, Un, lane, tok_lane, Gn);
+      rec_next = load_rec(L, item_at(w + 2) / ng, n_units);
       if (slot_has_lora(G)) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -295,7 +301,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             if (phase == 0) {                              // x rows of the unit's tokens
               ok = __all_sync(0xffffffffu, mbar_wait(bar_xempty, (xi & 1) ^ 1));
               if (!ok) break;
-              const bool mine = lane < U.n_tok;
+              const bool mine = lane < U.n_tok && G.tok[0] >= 0;
               const uint32_t rows = __popc(__ballot_sync(0xffffffffu, mine));
               if (lane == 0) mbar_arrive_expect_tx(bar_xfull, rows * fw * 2);
               __syncwarp();
@@ -339,16 +345,16 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
     const int mi = lane >> 3, ri = lane & 7;              // ldmatrix: matrix and row this lane addresses
     __nv_bfloat16* sb_hi = sb;
     __nv_bfloat16* sb_lo = sb + kUnitTok * kSbPitch;
-    int4 rec = load_rec(seg, item_at(0) / ng, n_units);
+    int4 rec = load_rec(L, item_at(0) / ng, n_units);
     Gathered G;
     Unit U = unit_of(L, rec, item_at(0) % ng);
-    gather_issue<4>(seg, U, lane, tok_store, G);
-    int4 rec_next = load_rec(seg, item_at(1) / ng, n_units);
+    gather_issue<4>(L, seg, U, lane, tok_store, G);
+    int4 rec_next = load_rec(L, item_at(1) / ng, n_units);
     for (int w = 0; item_at(w) < n_items; ++w) {
       const Unit Un = unit_of(L, rec_next, item_at(w + 1) % ng);
       Gathered Gn;
-      gather_issue<4>(seg, Un, lane, tok_store, Gn);
-      rec_next = load_rec(seg, item_at(w + 2) / ng, n_units);
+      gather_issue<4>(L, seg, Un, lane, tok_store, Gn);
+      rec_next = load_rec(L, item_at(w + 2) / ng, n_units);
       if (slot_has_lora(G)) {
         const uint64_t vm = valid_mask(G, U.r, L.num_pages, lane);
         const int ng = (U.r + 15) / 16;

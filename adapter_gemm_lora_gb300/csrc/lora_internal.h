@@ -69,7 +69,7 @@ struct lora_pool {
   std::vector<uint16_t> h_stage;
 
   // kernel accounting (lora_profile_*)
-  int64_t launches[LORA_N_KINDS] = {0, 0, 0, 0};
+  int64_t launches[LORA_N_KINDS] = {};
   bool prof_on = false;
   struct ProfRec { int kind; cudaEvent_t start, stop; };
   std::vector<ProfRec> prof_rec;
@@ -110,11 +110,30 @@ struct LoraLaunch {
   const int32_t* ptab;
   const int32_t* rank;
   const lora_segments* seg;
+  const int32_t* units;                // the work list: seg->units, or seg->units_rest when the
+  const int32_t* n_units;              // fused tiles take their LoRA term in the GEMM
+  const int32_t* tile_plan;            // non-null: tokens of fused tiles are skipped
   const uint16_t* x;
   int32_t* err;
   bool pdl;
 };
 int launch_lora_delta(const LoraLaunch& L, cudaStream_t st);
+
+// Shrink of the fused tiles (s = x A, for every group member of the call) into seg->s_lora.
+struct ShrinkLaunch {
+  const uint16_t* pool;
+  int64_t num_pages;
+  int32_t H, T, n_slots;
+  int32_t n_group;
+  int32_t slot[LORA_MAX_GROUP];
+  const int32_t* ptab;
+  const int32_t* rank;
+  const lora_segments* seg;
+  const uint16_t* x;
+  int32_t* err;
+  bool pdl;
+};
+int launch_lora_shrink(const ShrinkLaunch& S, cudaStream_t st);
 
 struct GemmLaunch {
   const uint16_t* x;       // [T][H]
@@ -128,8 +147,21 @@ struct GemmLaunch {
   int32_t T, H, slot, n_slots;
   int32_t* err;
   bool pdl;
+  // fused tiles of a prefill-shaped batch (launch_gemm_fused)
+  const int32_t* tile_plan;
+  const uint16_t* s_lora;  // [T][kSCols] bf16, this slot's s of the fused tiles
+  const uint16_t* pool;
+  int64_t num_pages;
+  const int32_t* rank;
+  float* lora_dbg;         // the LoRA-only launch writes the fp32 LoRA term of the fused tiles here
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
+// n (1 .. LORA_MAX_GROUP) slots that read the same x whose batch is cut into 256-token tiles on
+// the persistent GEMM: the fused tiles of the plan take their LoRA term inside the GEMM.
+// gemm_fused_fits says whether the geometry allows it; lora_only runs only that term, into
+// G[i].lora_dbg, for the fused tiles.
+bool gemm_fused_fits(const GemmLaunch* G, int n);
+int launch_gemm_fused(const GemmLaunch* G, int n, bool lora_only, cudaStream_t st);
 // n (2 .. LORA_MAX_GROUP) slots that read the same x, batches of <= 256 tokens: one persistent
 // split-K launch over every (slot, feature tile).  gemm_group_fits says whether the group
 // qualifies (split-K geometry, one x, scratch for n slots); otherwise launch_gemm per slot.
@@ -144,15 +176,34 @@ constexpr int64_t gemm_partial_floats(int32_t T_max, int32_t H) {
 // Byte offsets of the arrays of a segment workspace (lora_segments_init) for batches of up to
 // T_max tokens, hidden size H, adapter ids below max_adapters and group calls of up to
 // max_group slots; every array starts on a 256-byte boundary.
+// Fused tiles of prefill-shaped batches: tiles of 256 tokens with at most 4 adapters, whose
+// LoRA term the base GEMM adds from s = x A (bf16 hi and lo parts, 512 columns per token: tile
+// slot b's hi part in [128 b, 128 b + 64), its lo part in [128 b + 64, 128 b + 128)).
+constexpr int kTileTokens = LORA_TILE_TOKENS;
+constexpr int kTileAdapters = LORA_TILE_ADAPTERS;
+constexpr int kPlanStride = 8;                         // int32 per tile in tile_plan
+constexpr int kSCols = 2 * LORA_MAX_RANK * kTileAdapters;   // bf16 columns of s_lora per token
+// The shrink kernel's persistent clusters (4 CTAs, one K quarter each) exchange partial sums of
+// s through global scratch: per cluster and item parity, 4 owners x 3 senders x [64 tokens][128
+// rows] fp32.
+constexpr int kShrinkCluster = 4;
+constexpr int kShrinkMaxClusters = 40;
+constexpr size_t kShrinkScratchFloats =
+    (size_t)kShrinkMaxClusters * 2 * kShrinkCluster * (kShrinkCluster - 1) * 64 * 128;
+constexpr int32_t fused_tiles_max(int32_t T_max) { return T_max > kTileTokens ? (T_max + kTileTokens - 1) / kTileTokens : 0; }
+
 struct SegLayout {
-  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials, total;
-  int32_t max_seg, unit_cap;
+  size_t perm, seg_off, seg_adapter, n_seg, tok_adapter, units, n_units, delta, partials;
+  size_t tile_plan, entries, n_entries, units_rest, n_units_rest, s_lora, shrink_scratch, total;
+  int32_t max_seg, unit_cap, n_tiles_max;
 };
 constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 constexpr SegLayout segments_layout(int32_t T_max, int32_t H, int32_t max_adapters, int32_t max_group) {
   SegLayout L{};
   L.max_seg = T_max < max_adapters ? T_max : max_adapters;
   L.unit_cap = T_max / kUnitTokens + L.max_seg + 1;
+  L.n_tiles_max = fused_tiles_max(T_max);
+  const bool fused = L.n_tiles_max > 0;
   size_t off = 0;
   L.perm = off;         off = align256(off + (size_t)T_max * 4);
   L.seg_off = off;      off = align256(off + (size_t)(L.max_seg + 2) * 4);
@@ -163,6 +214,13 @@ constexpr SegLayout segments_layout(int32_t T_max, int32_t H, int32_t max_adapte
   L.n_units = off;      off = align256(off + 16);
   L.delta = off;        off = align256(off + (size_t)max_group * T_max * H * 4);
   L.partials = off;     off = align256(off + (size_t)max_group * gemm_partial_floats(T_max, H) * 4);
+  L.tile_plan = off;    off = align256(off + (size_t)L.n_tiles_max * kPlanStride * 4);
+  L.entries = off;      off = align256(off + (size_t)L.n_tiles_max * kTileAdapters * 4);
+  L.n_entries = off;    off = align256(off + (fused ? 16 : 0));
+  L.units_rest = off;   off = align256(off + (fused ? (size_t)L.unit_cap * 16 : 0));
+  L.n_units_rest = off; off = align256(off + (fused ? 16 : 0));
+  L.s_lora = off;       off = align256(off + (fused ? (size_t)max_group * T_max * kSCols * 2 : 0));
+  L.shrink_scratch = off; off = align256(off + (fused ? kShrinkScratchFloats * 4 : 0));
   L.total = off;
   return L;
 }

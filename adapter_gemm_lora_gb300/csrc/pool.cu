@@ -201,7 +201,7 @@ int lora_profile_enable(lora_pool* p, int32_t enable) {
 
 int lora_profile_read(lora_pool* p, int32_t n_kinds, int64_t* launches, double* ms, int32_t reset) {
   if (!p || n_kinds < 0 || (n_kinds > 0 && (!launches || !ms))) return lora_fail(LORA_EINVAL, "lora_profile_read: bad arguments");
-  double acc[LORA_N_KINDS] = {0, 0, 0, 0};
+  double acc[LORA_N_KINDS] = {};
   int rc = LORA_OK;
   for (auto& r : p->prof_rec) {
     float t = 0.f;
@@ -865,6 +865,15 @@ int lora_segments_init_group(const lora_pool* p, void* ws, int64_t ws_bytes, int
   seg->delta_slots = max_group;
   seg->delta = reinterpret_cast<float*>(b + L.delta);
   seg->gemm_partials = reinterpret_cast<float*>(b + L.partials);
+  const bool fused = L.n_tiles_max > 0;
+  seg->n_tiles_max = L.n_tiles_max;
+  seg->tile_plan = fused ? reinterpret_cast<int32_t*>(b + L.tile_plan) : nullptr;
+  seg->entries = fused ? reinterpret_cast<int32_t*>(b + L.entries) : nullptr;
+  seg->n_entries = fused ? reinterpret_cast<int32_t*>(b + L.n_entries) : nullptr;
+  seg->units_rest = fused ? reinterpret_cast<int32_t*>(b + L.units_rest) : nullptr;
+  seg->n_units_rest = fused ? reinterpret_cast<int32_t*>(b + L.n_units_rest) : nullptr;
+  seg->s_lora = fused ? reinterpret_cast<uint16_t*>(b + L.s_lora) : nullptr;
+  seg->shrink_scratch = fused ? reinterpret_cast<float*>(b + L.shrink_scratch) : nullptr;
   return LORA_OK;
 }
 

@@ -170,6 +170,86 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
       __syncthreads();
     }
   }
+  if (seg.tile_plan == nullptr || T <= kTileTokens) return;
+
+  // 4. tile plan of a prefill-shaped batch: the distinct adapters of every 256-token tile.  In
+  //    perm (adapter-major, token order inside an adapter) the tokens of one adapter in one tile
+  //    are a run; each run start names one (tile, adapter) pair.  Tiles with at most
+  //    kTileAdapters adapters are fused, their adapters listed in ascending id order.
+  __shared__ int32_t tile_cnt[LORA_MAX_TOKENS / kTileTokens];
+  __shared__ int32_t tile_ad[LORA_MAX_TOKENS / kTileTokens][kTileAdapters];
+  const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
+  for (int i = tid; i < n_tiles; i += kThreads) tile_cnt[i] = 0;
+  __syncthreads();
+  const int off0 = cnt[0];                     // the no-adapter tokens come first in perm
+  for (int i = off0 + tid; i < T; i += kThreads) {
+    const int32_t t = seg.perm[i];
+    const int32_t a = seg.tok_adapter[t];
+    bool first = i == off0;
+    if (!first) {
+      const int32_t tp = seg.perm[i - 1];
+      first = seg.tok_adapter[tp] != a || (tp / kTileTokens) != (t / kTileTokens);
+    }
+    if (first) {
+      const int tile = t / kTileTokens;
+      const int b = atomicAdd(&tile_cnt[tile], 1);
+      if (b < kTileAdapters) tile_ad[tile][b] = a;
+    }
+  }
+  __syncthreads();
+  int32_t ev[4] = {0, 0, 0, 0};                // fused (tile, adapter) pairs of this thread's tile
+  int32_t nb = 0;
+  if (tid < n_tiles) {
+    nb = tile_cnt[tid] <= kTileAdapters ? tile_cnt[tid] : -1;
+    int32_t ad[kTileAdapters];
+#pragma unroll
+    for (int b = 0; b < kTileAdapters; ++b) ad[b] = b < nb ? tile_ad[tid][b] : -1;
+#pragma unroll
+    for (int i = 1; i < kTileAdapters; ++i)    // insertion sort of at most 4 ids
+#pragma unroll
+      for (int j = i; j > 0; --j)
+        if (j < nb && ad[j - 1] > ad[j]) {
+          const int32_t x = ad[j - 1];
+          ad[j - 1] = ad[j];
+          ad[j] = x;
+        }
+    int32_t* pl = seg.tile_plan + (size_t)tid * kPlanStride;
+    pl[0] = nb;
+#pragma unroll
+    for (int b = 0; b < kTileAdapters; ++b) pl[1 + b] = ad[b];
+    ev[0] = nb > 0 ? nb : 0;
+  }
+  for (int i = n_tiles + tid; i < seg.n_tiles_max; i += kThreads) seg.tile_plan[(size_t)i * kPlanStride] = -1;
+  int32_t etot[4];
+  block_exclusive_scan4(ev, sh_scan, etot);    // also orders the tile_cnt reads before the rewrite below
+  if (tid < n_tiles) {
+    for (int b = 0; b < nb; ++b) seg.entries[ev[0] + b] = tid * kTileAdapters + b;
+    tile_cnt[tid] = nb;                        // from here on: < 0 marks a tile that is not fused
+  }
+  if (tid == 0) *seg.n_entries = etot[0];
+  __syncthreads();
+
+  // 5. the work units the LoRA-delta kernel still has to do when the fused tiles take their
+  //    LoRA term in the GEMM: those holding a token of a tile that is not fused, kept in order.
+  const int32_t n_units = utot[0] + utot[1] + utot[2] + utot[3];
+  const int u_per = (n_units + kThreads - 1) / kThreads;
+  const int u_lo = min(n_units, tid * u_per), u_hi = min(n_units, u_lo + u_per);
+  int32_t lv[4] = {0, 0, 0, 0};
+  uint32_t live_bits = 0;                      // u_per <= 32 for every T <= LORA_MAX_TOKENS
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int4 rec = reinterpret_cast<const int4*>(seg.units)[u];
+    bool live = false;
+    for (int j = 0; j < rec.w && !live; ++j) live = tile_cnt[seg.perm[rec.z + j] / kTileTokens] < 0;
+    if (live) {
+      live_bits |= 1u << (u - u_lo);
+      ++lv[0];
+    }
+  }
+  int32_t ltot[4];
+  block_exclusive_scan4(lv, sh_scan, ltot);
+  for (int u = u_lo, pos = lv[0]; u < u_hi; ++u)
+    if ((live_bits >> (u - u_lo)) & 1u) reinterpret_cast<int4*>(seg.units_rest)[pos++] = reinterpret_cast<const int4*>(seg.units)[u];
+  if (tid == 0) *seg.n_units_rest = ltot[0];
 }
 
 }  // namespace

@@ -108,7 +108,26 @@ typedef struct lora_segments {
   float*   gemm_partials; /* [delta_slots][3][P][H] fp32 partial sums of the base GEMM for batches
                              of <= 256 tokens (K split over 4 CTAs); P = min(T_max, 256) rounded
                              up to 128 */
+  /* Batches of more than 256 tokens (prefill-shaped; empty when T_max <= 256): the batch is cut
+   * into tiles of 256 consecutive tokens, and a tile whose tokens carry at most
+   * LORA_TILE_ADAPTERS distinct adapters ("a fused tile") gets its LoRA term inside the base
+   * GEMM (see lora_linear_forward).  After a build: */
+  int32_t  n_tiles_max;   /* capacity: T_max / 256 rounded up (0 when T_max <= 256) */
+  int32_t* tile_plan;     /* [n_tiles_max][8]: [0] = adapters of tile i, or -1 when it has more than
+                             LORA_TILE_ADAPTERS; [1..4] their ids, ascending */
+  int32_t* entries;       /* [4 * n_tiles_max]: the fused (tile, adapter slot b) pairs, tile * 4 + b,
+                             in tile order */
+  int32_t* n_entries;
+  int32_t* units_rest;    /* [4 * unit_cap]: the work units (same records as units) that hold at
+                             least one token of a non-fused tile, in the order of units */
+  int32_t* n_units_rest;
+  uint16_t* s_lora;       /* [delta_slots][T_max][512] bf16: per token of a fused tile, s = x A of
+                             its adapter as hi and lo bf16 parts in the columns of its tile slot */
+  float*   shrink_scratch;/* fp32 partial sums exchanged by the shrink kernel's CTAs */
 } lora_segments;
+
+#define LORA_TILE_TOKENS   256      /* tokens per tile of a prefill-shaped batch */
+#define LORA_TILE_ADAPTERS 4        /* distinct adapters a fused tile may carry */
 
 /*
  * Create a pool over caller-owned device storage.
@@ -350,7 +369,7 @@ const char* lora_last_error(void);
 /*
  * Kernel accounting for benchmarks.  Every kernel this library launches for `pool` is counted
  * by kind: 0 segment build, 1 LoRA delta (shrink and expand), 2 base GEMM, 3 page scatter
- * (adapter loads).
+ * (adapter loads), 4 shrink of the fused tiles of a prefill-shaped batch.
  * With profiling enabled, each launch is also bracketed by CUDA events recorded on the
  * stream it runs on (also inside a stream capture: the events then become graph nodes and
  * are re-recorded by every replay).  lora_profile_read synchronises those events and
@@ -362,7 +381,8 @@ const char* lora_last_error(void);
 #define LORA_KIND_DELTA    1
 #define LORA_KIND_GEMM     2
 #define LORA_KIND_SCATTER  3
-#define LORA_N_KINDS       4
+#define LORA_KIND_SHRINK   4
+#define LORA_N_KINDS       5
 int lora_profile_enable(lora_pool* pool, int32_t enable);
 int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, double* ms_host,
                       int32_t reset);

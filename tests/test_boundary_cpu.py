@@ -201,7 +201,9 @@ def test_group_workspace_sizes_and_argument_checks(L):
     pool = L.lora_pool_create(None, 10, H, 4, 1)
     one = L.lora_segments_size(pool, T)
     assert L.lora_segments_size_group(pool, T, 1) == one
-    per_slot = T * H * 4 + 3 * 256 * H * 4           # fp32 delta + split-K scratch (3 tiles of 256 tokens)
+    # fp32 delta + split-K scratch (3 tiles of 256 tokens) + the fused tiles' s (512 bf16 per token;
+    # batches of more than 256 tokens)
+    per_slot = T * H * 4 + 3 * 256 * H * 4 + T * 512 * 2
     for g in (2, 3, 4):
         assert L.lora_segments_size_group(pool, T, g) - one == (g - 1) * per_slot
     for g in (0, L.LORA_MAX_GROUP + 1):
@@ -415,3 +417,21 @@ def test_noalloc_scratch_holds_a_workspace_at_its_limits(L):
         assert need <= L.LORA_NOALLOC_SCRATCH_BYTES
     finally:
         L.lora_pool_destroy(pool)
+
+
+def test_segments_struct_layout_matches_the_header(L, tmp_path):
+    """The binding's ctypes mirror of lora_segments has the C struct's size and field offsets."""
+    import ctypes
+    fields = [f for f, _ in L.lora_segments._fields_]
+    body = "".join(f'printf("%s %zu\\n", "{f}", offsetof(lora_segments, {f}));' for f in fields)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "lora.h"\n'
+                   'int main(void){' + body + 'printf("size %zu\\n", sizeof(lora_segments)); return 0;}\n')
+    exe = tmp_path / "layout"
+    r = subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    for f in fields:
+        assert int(out[f]) == getattr(L.lora_segments, f).offset, f
+    assert int(out["size"]) == ctypes.sizeof(L.lora_segments)

@@ -256,3 +256,26 @@ def small(H: int, T: int, n_adapters: int, ranks, seed: int, n_slots: int = 1,
     return Workload(spec=spec, seed=seed, ranks=ranks, req_adapter=token_adapter.copy(),
                     req_len=np.ones(T, dtype=np.int32), token_adapter=token_adapter,
                     page_order=page_order, kv_pages=int(kv_fill * pool_pages))
+
+
+def small_prefill(H: int, req_lens, n_adapters: int, ranks, seed: int, n_slots: int = 1,
+                  kv_fill: float = 0.25, none_reqs=(), n_decode: int = 0) -> Workload:
+    """A small prefill-shaped workload: `n_decode` one-token requests with uniform adapters, then
+    one request per entry of `req_lens`, all of whose tokens carry that request's adapter (drawn
+    uniformly; requests listed in `none_reqs` carry none, -1)."""
+    rng = np.random.default_rng(seed)
+    ranks = np.array(ranks, dtype=np.int32)
+    assert ranks.shape[0] == n_adapters
+    lens = np.array([1] * n_decode + list(req_lens), dtype=np.int32)
+    req_adapter = rng.integers(0, n_adapters, size=lens.size).astype(np.int32)
+    for i in none_reqs:
+        req_adapter[n_decode + i] = -1
+    token_adapter = np.repeat(req_adapter, lens).astype(np.int32)
+    T = int(lens.sum())
+    need = int(2 * ranks.astype(np.int64).sum() * n_slots)
+    pool_pages = int((need + 16) / max(1e-9, 1.0 - kv_fill)) + 8
+    page_order = rng.permutation(pool_pages).astype(np.int64)
+    spec = Spec(0, "small_prefill", H=H, n_slots=n_slots, n_adapters=n_adapters, pool_pages=pool_pages,
+                kv_fill=kv_fill, assign="uniform", n_decode=T)
+    return Workload(spec=spec, seed=seed, ranks=ranks, req_adapter=req_adapter, req_len=lens,
+                    token_adapter=token_adapter, page_order=page_order, kv_pages=int(kv_fill * pool_pages))
