@@ -49,8 +49,8 @@ EXPORTED = ["lora_pool_create", "lora_pool_reserve", "lora_pool_release", "lora_
             "lora_adapter_acquire", "lora_adapter_release", "lora_adapter_refs", "lora_pool_evict_idle",
             "lora_adapter_ensure", "lora_pool_set_eviction", "lora_adapter_packed_size", "lora_adapter_pack",
             "lora_adapter_load_packed", "lora_adapter_wait", "lora_kv_grow", "lora_kv_free", "lora_kv_length",
-            "lora_kv_table"]
-KINDS = ("segments", "delta", "gemm", "scatter", "shrink")
+            "lora_kv_table", "lora_kv_batch_table", "lora_attention_decode"]
+KINDS = ("segments", "delta", "gemm", "scatter", "shrink", "attention")
 
 
 class LoraError(RuntimeError):
@@ -123,6 +123,8 @@ def _load():
         "lora_kv_free": (I32, [VP, I64]),
         "lora_kv_length": (I64, [VP, I64]),
         "lora_kv_table": (I32, [VP, I64, I32, VP]),
+        "lora_kv_batch_table": (I32, [VP, VP, I32, I32, VP, VP, VP]),
+        "lora_attention_decode": (I32, [VP, I32, VP, VP, I32, I32, I32, VP, VP, I32, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -298,6 +300,20 @@ def lora_kv_table(pool, request_id: int, layer: int) -> np.ndarray:
     out = np.zeros((max(n, 1), 2), dtype=np.int32)
     _check(_load().lora_kv_table(pool, request_id, layer, _ptr(out)))
     return out[:n]
+
+
+def lora_kv_batch_table(pool, request_ids, max_len: int, table_dev, seq_len_dev, stream=None) -> None:
+    """Every request's KV page list (as lora_kv_grow took it) into table_dev, lengths into seq_len_dev."""
+    ids = np.ascontiguousarray(request_ids, dtype=np.int64)
+    _check(_load().lora_kv_batch_table(pool, _ptr(ids) if ids.size else None, ids.size, max_len, _ptr(table_dev),
+                                       _ptr(seq_len_dev), _stream(stream)))
+
+
+def lora_attention_decode(pool, n_req: int, table_dev, seq_len_dev, max_len: int, layers: int, layer: int, q_dev,
+                          out_dev, n_heads: int, stream=None) -> None:
+    """Decode attention of one new token per request over its KV pages at `layer`."""
+    _check(_load().lora_attention_decode(pool, n_req, _ptr(table_dev), _ptr(seq_len_dev), max_len, layers, layer,
+                                         _ptr(q_dev), _ptr(out_dev), n_heads, _stream(stream)))
 
 
 def lora_adapter_refs(pool, adapter_id: int) -> int:

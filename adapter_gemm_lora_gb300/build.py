@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblora.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["pool.cu", "segments.cu", "lora_gather.cu", "lora_shrink.cu", "gemm_tcgen05.cu", "forward.cu", "noalloc.cu"]
+SOURCES = ["pool.cu", "segments.cu", "lora_gather.cu", "lora_shrink.cu", "gemm_tcgen05.cu", "forward.cu", "noalloc.cu",
+           "attention.cu"]
 
 
 def _nvcc() -> str:

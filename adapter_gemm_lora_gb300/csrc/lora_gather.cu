@@ -150,6 +150,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 // and lane + 32 (-1 past the rank) and perm entries.
 struct Unit {
   int r, t_begin, n_tok;
+  bool mixed;              // some of its tokens belong to fused tiles (skipped here)
   const int32_t* tab;      // the adapter's page table on the item's slot
   float* delta;            // the slot's delta rows
 };
@@ -161,7 +162,8 @@ __device__ __forceinline__ Unit unit_of(const LoraLaunch& L, const int4& rec, in
   Unit U;
   U.r = rec.y;
   U.t_begin = rec.z;
-  U.n_tok = rec.w;
+  U.n_tok = rec.w & (kUnitMixed - 1);
+  U.mixed = (rec.w & kUnitMixed) != 0;
   int slot = L.slot[0];
   float* d = L.delta[0];
 #pragma unroll
@@ -195,7 +197,7 @@ __device__ __forceinline__ void gather_issue(const LoraLaunch& L, const lora_seg
     const int t = tok_index(lane, k);
     G.tok[k] = t < U.n_tok ? __ldg(seg.perm + U.t_begin + t) : -1;
   }
-  if (L.tile_plan != nullptr) {
+  if (L.tile_plan != nullptr && U.mixed) {
 #pragma unroll
     for (int k = 0; k < NTOK; ++k)
       if (G.tok[k] >= 0 && __ldg(L.tile_plan + (size_t)(G.tok[k] / kTileTokens) * kPlanStride) >= 0) G.tok[k] = -1;

@@ -24,6 +24,7 @@ enum : int32_t {
 constexpr int kTabStride = 2 * LORA_MAX_RANK;
 // Work-list geometry shared by the segment builder and the gather kernels.
 constexpr int kUnitTokens = 16;      // tokens per LoRA-delta work unit
+constexpr int kUnitMixed = 1 << 8;   // in units_rest: the unit also holds tokens of fused tiles
 
 struct lora_pool {
   void* pool_dev = nullptr;
@@ -54,6 +55,7 @@ struct lora_pool {
     std::vector<int32_t> pages;                   // per token: per layer, K page then V page
   };
   std::unordered_map<int64_t, KVReq> kv;          // request id -> its KV pages
+  std::vector<int32_t> h_kvtab;                   // host staging of lora_kv_batch_table
   std::vector<int32_t> future;                    // upcoming adapter requests (farthest-future rule)
   int32_t lookahead = 0;                          // entries of `future` looked at; <= 0: all
   int64_t adapter_pages = 0;

@@ -108,6 +108,10 @@ lora_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, ShrinkParams p) {
   const int cluster_id = (int)blockIdx.x / KS;
   const int kb_lo = me * p.n_kb / KS, kb_hi = (me + 1) * p.n_kb / KS;
   const int nk = kb_hi - kb_lo;                              // >= 1: the launcher requires n_kb >= 4
+  pdl_wait_then_release();                                   // the plan comes from the segment build
+  const int n_pairs = (p.n_group + 1) / 2;
+  const int n_items = *p.n_entries * n_pairs;
+  if (cluster_id >= n_items) return;                         // the whole cluster: nothing to do
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -132,9 +136,6 @@ lora_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, ShrinkParams p) {
   tc_fence_after();
   cluster_sync_all();                                        // peers' barriers exist before any remote arrive
   const uint32_t tmem = *tmem_slot;
-  pdl_wait_then_release();                                   // the plan comes from the segment build
-  const int n_pairs = (p.n_group + 1) / 2;
-  const int n_items = *p.n_entries * n_pairs;
 
   if (warp == 0) {
     if (lane == 0) {                                         // TMA: the tile's x rows, K quarter

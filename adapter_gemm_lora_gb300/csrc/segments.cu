@@ -230,25 +230,36 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   __syncthreads();
 
   // 5. the work units the LoRA-delta kernel still has to do when the fused tiles take their
-  //    LoRA term in the GEMM: those holding a token of a tile that is not fused, kept in order.
+  //    LoRA term in the GEMM: those holding a token of a tile that is not fused, kept in order;
+  //    a unit that also holds tokens of fused tiles gets kUnitMixed in its token count, so the
+  //    delta kernel looks tiles up only for such units.
   const int32_t n_units = utot[0] + utot[1] + utot[2] + utot[3];
   const int u_per = (n_units + kThreads - 1) / kThreads;
   const int u_lo = min(n_units, tid * u_per), u_hi = min(n_units, u_lo + u_per);
   int32_t lv[4] = {0, 0, 0, 0};
-  uint32_t live_bits = 0;                      // u_per <= 32 for every T <= LORA_MAX_TOKENS
+  uint32_t live_bits = 0, mixed_bits = 0;      // u_per <= 32 for every T <= LORA_MAX_TOKENS
   for (int u = u_lo; u < u_hi; ++u) {
     const int4 rec = reinterpret_cast<const int4*>(seg.units)[u];
-    bool live = false;
-    for (int j = 0; j < rec.w && !live; ++j) live = tile_cnt[seg.perm[rec.z + j] / kTileTokens] < 0;
+    bool live = false, fused = false;
+    for (int j = 0; j < rec.w; ++j) {
+      const bool f = tile_cnt[seg.perm[rec.z + j] / kTileTokens] >= 0;
+      live = live || !f;
+      fused = fused || f;
+    }
     if (live) {
       live_bits |= 1u << (u - u_lo);
+      if (fused) mixed_bits |= 1u << (u - u_lo);
       ++lv[0];
     }
   }
   int32_t ltot[4];
   block_exclusive_scan4(lv, sh_scan, ltot);
   for (int u = u_lo, pos = lv[0]; u < u_hi; ++u)
-    if ((live_bits >> (u - u_lo)) & 1u) reinterpret_cast<int4*>(seg.units_rest)[pos++] = reinterpret_cast<const int4*>(seg.units)[u];
+    if ((live_bits >> (u - u_lo)) & 1u) {
+      int4 rec = reinterpret_cast<const int4*>(seg.units)[u];
+      if ((mixed_bits >> (u - u_lo)) & 1u) rec.w |= kUnitMixed;
+      reinterpret_cast<int4*>(seg.units_rest)[pos++] = rec;
+    }
   if (tid == 0) *seg.n_units_rest = ltot[0];
 }
 

@@ -400,6 +400,56 @@ class Harness:
         return times, h2d, d2h
 
 
+def attention_leg(L, H, device, n_req=256, ctx=(128, 2048), head_dim=128, calls=30, seed=7):
+    """Paged decode attention over KV pages of a unified pool (the pool's second consumer): one new
+    token per request at one layer, contexts uniform in `ctx` (seeded), KV pages taken by
+    lora_kv_grow in a seeded page order.  HBM roofline: every cached K and V page row is read
+    once (2 x context x H x 2 bytes per request) plus q and out.  Inputs (GBs of KV) are far
+    larger than L2, so no flush is needed between calls."""
+    import torch
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(ctx[0], ctx[1] + 1, size=n_req)
+    num_pages = int(2 * lens.sum()) + 64
+    pool_t = torch.empty((num_pages, H), dtype=torch.bfloat16, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    pool_t.normal_(generator=g)
+    pool = L.lora_pool_create(pool_t, num_pages, H, 1, 1, rng.permutation(num_pages))
+    try:
+        for r, n in enumerate(lens):
+            L.lora_kv_grow(pool, r, int(n), 1)
+        max_len = int(lens.max())
+        table = torch.empty((n_req, max_len, 1, 2), dtype=torch.int32, device=device)
+        seq = torch.empty(n_req, dtype=torch.int32, device=device)
+        L.lora_kv_batch_table(pool, np.arange(n_req), max_len, table, seq)
+        q = torch.randn((n_req, H), generator=g, device=device).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        n_heads = H // head_dim
+        stream = torch.cuda.current_stream(device).cuda_stream
+        for _ in range(3):
+            L.lora_attention_decode(pool, n_req, table, seq, max_len, 1, 0, q, out, n_heads, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(calls):
+            L.lora_attention_decode(pool, n_req, table, seq, max_len, 1, 0, q, out, n_heads, stream=stream)
+        e1.record()
+        torch.cuda.synchronize()
+        L.lora_status(pool)
+        us = e0.elapsed_time(e1) * 1e3 / calls
+        nbytes = int(2 * lens.sum()) * H * 2 + 2 * n_req * H * 2
+        peaks = load_peaks()
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"kernel": "attention_decode_kernel", "requests": n_req, "H": H, "head_dim": head_dim,
+                "context": f"uniform [{ctx[0]}, {ctx[1]}], mean {lens.mean():.0f}", "us_per_call": round(us, 2),
+                "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm"}
+    finally:
+        L.lora_pool_destroy(pool)
+        del pool_t
+        torch.cuda.empty_cache()
+
+
 def default_steps(key):
     return {1: 2000, 2: 8000, 3: 400, 4: 2000, 5: 40}[key]
 
@@ -420,6 +470,7 @@ def run_ours(args):
     res = h.run_timed(steps, args.warmup, dist)
     clocks.stop()
     e2e_times, h2d, d2h = h.run_e2e(min(steps, 200 if key != 5 else 10))
+    attention = attention_leg(h.L, wl.H, device) if not args.no_attention else None
     total_ms = sum(res["step_ms"])
     total_ms_max = max_over_ranks(total_ms, dist, device)
     T = wl.T
@@ -500,6 +551,8 @@ def run_ours(args):
                 "path": "eager public API calls, pinned host buffers"},
         "clocks": clocks.summary(res["t0"] - 1.5, res["t1"]),
     }
+    if attention is not None:
+        line["attention_decode"] = attention
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     if rank == 0:
@@ -649,6 +702,7 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-attention", action="store_true", help="skip the paged decode attention leg")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     rc = check_world(args.gpus, argv)

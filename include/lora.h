@@ -118,8 +118,10 @@ typedef struct lora_segments {
   int32_t* entries;       /* [4 * n_tiles_max]: the fused (tile, adapter slot b) pairs, tile * 4 + b,
                              in tile order */
   int32_t* n_entries;
-  int32_t* units_rest;    /* [4 * unit_cap]: the work units (same records as units) that hold at
-                             least one token of a non-fused tile, in the order of units */
+  int32_t* units_rest;    /* [4 * unit_cap]: the work units (records as in units) that hold at
+                             least one token of a non-fused tile, in the order of units; the token
+                             count of a unit that also holds tokens of fused tiles has bit 8 (256)
+                             set */
   int32_t* n_units_rest;
   uint16_t* s_lora;       /* [delta_slots][T_max][512] bf16: per token of a fused tile, s = x A of
                              its adapter as hi and lo bf16 parts in the columns of its tile slot */
@@ -172,6 +174,27 @@ int lora_kv_grow(lora_pool* pool, int64_t request_id, int32_t n_tokens, int32_t 
 int lora_kv_free(lora_pool* pool, int64_t request_id);
 int64_t lora_kv_length(const lora_pool* pool, int64_t request_id);
 int lora_kv_table(const lora_pool* pool, int64_t request_id, int32_t layer, int32_t* table_host);
+
+/*
+ * Decode attention over KV pages of the pool ("Unified paging": a token's K and V at each layer
+ * are one page each, so adapter pages and KV pages share one pool and one free list).  For one
+ * new token per request, at `layer`, per head h of width D = H / n_heads (D = 64 or 128):
+ *     out_h = softmax_j( q_h . K_{j,h} / sqrt(D) ) V_{j,h}      over the request's cached tokens j
+ * (plain scaled dot-product attention; the pages give no formula of their own).
+ *   lora_kv_batch_table: writes table_dev (device int32 [n_req][max_len][layers][2]: every
+ *     request's KV page list as lora_kv_grow took it, -1 past its length) and seq_len_dev
+ *     (device int32 [n_req]); every request must hold pages, with one layer count, and at most
+ *     max_len tokens (LORA_EINVAL otherwise).  Synchronises `stream` (its host staging is reused).
+ *   lora_attention_decode: q and out device bf16 [n_req][H] (16-byte aligned); out is rounded
+ *     to bf16 once from fp32.  A request with no cached token gets zeros.  Page ids outside the
+ *     pool set the device error word (lora_status) and their tokens are skipped.  One kernel;
+ *     at most 65535 requests per call.
+ */
+int lora_kv_batch_table(lora_pool* pool, const int64_t* request_ids_host, int32_t n_req, int32_t max_len,
+                        int32_t* table_dev, int32_t* seq_len_dev, lora_stream_t stream);
+int lora_attention_decode(lora_pool* pool, int32_t n_req, const int32_t* table_dev, const int32_t* seq_len_dev,
+                          int32_t max_len, int32_t layers, int32_t layer, const void* q, void* out, int32_t n_heads,
+                          lora_stream_t stream);
 
 /* Give back n reserved pages (appended to the free list in the order given).
  * LORA_EINVAL if any id is not currently reserved or appears twice (nothing released). */
@@ -369,7 +392,7 @@ const char* lora_last_error(void);
 /*
  * Kernel accounting for benchmarks.  Every kernel this library launches for `pool` is counted
  * by kind: 0 segment build, 1 LoRA delta (shrink and expand), 2 base GEMM, 3 page scatter
- * (adapter loads), 4 shrink of the fused tiles of a prefill-shaped batch.
+ * (adapter loads), 4 shrink of the fused tiles of a prefill-shaped batch, 5 decode attention.
  * With profiling enabled, each launch is also bracketed by CUDA events recorded on the
  * stream it runs on (also inside a stream capture: the events then become graph nodes and
  * are re-recorded by every replay).  lora_profile_read synchronises those events and
@@ -382,7 +405,8 @@ const char* lora_last_error(void);
 #define LORA_KIND_GEMM     2
 #define LORA_KIND_SCATTER  3
 #define LORA_KIND_SHRINK   4
-#define LORA_N_KINDS       5
+#define LORA_KIND_ATTENTION 5
+#define LORA_N_KINDS       6
 int lora_profile_enable(lora_pool* pool, int32_t enable);
 int lora_profile_read(lora_pool* pool, int32_t n_kinds, int64_t* launches_host, double* ms_host,
                       int32_t reset);

@@ -39,7 +39,11 @@ def plan_reference(ta, units, perm):
         ids = sorted({int(a) for a in ta[i * TILE:(i + 1) * TILE] if a >= 0})
         plan.append(ids if len(ids) <= 4 else None)
     entries = [4 * i + b for i, ids in enumerate(plan) if ids is not None for b in range(len(ids))]
-    rest = [tuple(u) for u in units if any(plan[perm[u[2] + k] // TILE] is None for k in range(u[3]))]
+    rest = []
+    for u in units:
+        fused = [plan[perm[u[2] + k] // TILE] is not None for k in range(u[3])]
+        if not all(fused):                 # holds a token of an unfused tile; bit 8: also fused tokens
+            rest.append((u[0], u[1], u[2], u[3] | (256 if any(fused) else 0)))
     return plan, entries, rest
 
 
