@@ -450,6 +450,81 @@ def attention_leg(L, H, device, n_req=256, ctx=(128, 2048), head_dim=128, calls=
         torch.cuda.empty_cache()
 
 
+def prefetch_leg(device, n_steps=256, loads=(0, 16, 64, 256)):
+    """Adapter loads overlapped with compute ("S-LoRA, in depth", "Scheduling": pinned host memory and
+    a copy stream let the next batch's adapters load while the current batch computes; "Fewer
+    Expert Transfers Without Changing Routing", Eq. (1): a step costs c + rho tau with blocking
+    copies, and at best max(c, rho tau) when they overlap compute).
+
+    On the decode workload (one layer's q/k/v/o, 256 tokens): c = the step alone (graph replay);
+    tau = one packed load of the largest adapter the batch does not use (pinned host memory,
+    lora_adapter_load_packed on a copy stream) alone; then n_steps steps replayed on the compute
+    stream while the copy stream loads and unloads that adapter `m` times (rho = m / n_steps).
+    The load kernel reads host memory with SM threads, so it also takes SMs from the steps."""
+    import torch
+    h = Harness(2, device)
+    L, wl = h.L, h.wl
+    S = wl.n_slots
+    used = set(int(a) for a in wl.token_adapter if a >= 0)
+    spare = max((a for a in range(wl.spec.n_adapters) if a not in used), key=lambda a: int(wl.ranks[a]))
+    r = int(wl.ranks[spare])
+    A = [wl.A(spare, s) for s in range(S)]
+    B = [wl.B(spare, s) for s in range(S)]
+    nbytes = L.lora_adapter_packed_size(h.pool, r)
+    buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    L.lora_adapter_pack(h.pool, r, A, B, buf, nbytes)
+    compute = torch.cuda.Stream(device=device)
+    copy = torch.cuda.Stream(device=device)
+    L.lora_adapter_unload(h.pool, spare, stream=compute.cuda_stream)
+    with torch.cuda.stream(compute):
+        for _ in range(5):
+            h.step(compute.cuda_stream)
+    chunk = 32
+    g, g_events = h.capture(chunk, compute)       # the graph records these events: keep them alive
+    torch.cuda.synchronize()
+
+    def cycle(n):
+        for _ in range(n):
+            L.lora_adapter_load_packed(h.pool, spare, r, buf, nbytes, S, copy_stream=copy.cuda_stream)
+            L.lora_adapter_unload(h.pool, spare, stream=copy.cuda_stream)
+
+    cycle(3)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(copy)
+    cycle(32)
+    e1.record(copy)
+    torch.cuda.synchronize()
+    tau = e0.elapsed_time(e1) / 32
+    rows = []
+    for m in loads:
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0 = torch.cuda.Event(enable_timing=True)
+        c0.record(compute)
+        k0.record(copy)
+        with torch.cuda.stream(compute):
+            for _ in range(n_steps // chunk):
+                g.replay()
+        c1.record(compute)
+        cycle(m)
+        torch.cuda.synchronize()
+        c_ms = c0.elapsed_time(c1) / n_steps
+        rows.append({"loads": m, "rho": round(m / n_steps, 4), "step_ms": round(c_ms, 5)})
+    c = rows[0]["step_ms"]
+    for row in rows:
+        rt = row["rho"] * tau
+        row["blocking_model_ms"] = round(c + rt, 5)
+        row["overlap_model_ms"] = round(max(c, rt), 5)
+    L.lora_status(h.pool)
+    del g, g_events
+    L.lora_pool_destroy(h.pool)
+    return {"workload": wl.spec.name, "adapter_rank": r, "adapter_bytes": int(2 * r * S * wl.H * 2),
+            "tau_ms": round(tau, 5), "c_ms": c, "rows": rows,
+            "note": "steps replayed on the compute stream while the copy stream loads and unloads one packed "
+                    "adapter m times; tau includes the unload"}
+
+
 def default_steps(key):
     return {1: 2000, 2: 8000, 3: 400, 4: 2000, 5: 40}[key]
 
@@ -471,6 +546,7 @@ def run_ours(args):
     clocks.stop()
     e2e_times, h2d, d2h = h.run_e2e(min(steps, 200 if key != 5 else 10))
     attention = attention_leg(h.L, wl.H, device) if not args.no_attention else None
+    prefetch = prefetch_leg(device) if args.prefetch else None
     total_ms = sum(res["step_ms"])
     total_ms_max = max_over_ranks(total_ms, dist, device)
     T = wl.T
@@ -553,6 +629,8 @@ def run_ours(args):
     }
     if attention is not None:
         line["attention_decode"] = attention
+    if prefetch is not None:
+        line["adapter_prefetch"] = prefetch
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     if rank == 0:
@@ -703,6 +781,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-attention", action="store_true", help="skip the paged decode attention leg")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="also measure decode steps with adapter loads on a copy stream")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     rc = check_world(args.gpus, argv)
