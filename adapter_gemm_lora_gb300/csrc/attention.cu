@@ -9,9 +9,9 @@
 //
 // One CTA per (request, head), four warps splitting the cached tokens (token j to warp j % 4).
 // Lane l holds dimensions [l * D/32, (l+1) * D/32) of the head: the head's slice of a K or V page
-// is 2 D contiguous bytes, one coalesced load per warp.  The loop is bound by load latency, so a
-// warp issues the page ids and then the K and V slices of its next kBatch tokens before using
-// any of them.  Each warp keeps a running maximum, the running sum of exp(s - max) and an fp32
+// is 2 D contiguous bytes, one coalesced load per warp.  The loop is bound by load latency: the
+// CTA stages the page ids of kChunk tokens at a time in shared memory (one coalesced pass), and a
+// warp issues the K and V slices of its next kBatch tokens before using any of them.  Each warp keeps a running maximum, the running sum of exp(s - max) and an fp32
 // accumulator of V, rescaled when the maximum grows, taking its tokens in ascending order; the
 // four warps' partial results merge in shared memory in warp order, and the output is rounded
 // to bf16 once.  HBM-bound: 2 x tokens x 2 D bytes per (request, head).  Page ids are checked
@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kBatch = 4;                          // tokens a warp has in flight
+constexpr int kChunk = 512;                        // tokens whose page ids are staged at a time
 
 __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
   atomicCAS(err, 0, LORA_EDEVICE);
@@ -61,6 +62,7 @@ attention_decode_kernel(const uint16_t* __restrict__ pool, int64_t num_pages, in
   constexpr int VPL = D / 32;
   __shared__ float s_m[kWarps], s_l[kWarps];
   __shared__ float s_acc[kWarps][D];
+  __shared__ int32_t s_ids[kChunk][2];               // (K page, V page) of the chunk's tokens
   const int req = blockIdx.y, h = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n = seq_len[req];
@@ -75,46 +77,55 @@ attention_decode_kernel(const uint16_t* __restrict__ pool, int64_t num_pages, in
 #pragma unroll
   for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
   const int32_t* tab = table + (int64_t)req * max_len * layers * 2;
-  for (int j0 = warp; j0 < n; j0 += kWarps * kBatch) {
-    // tokens j0, j0 + 4, ..., j0 + 4 (kBatch - 1) of this warp: ids, then slices, then the math
-    bool ok[kBatch];
-    int32_t kp[kBatch], vp[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kWarps;
-      kp[u] = vp[u] = -1;
-      if (j < n) {
-        kp[u] = tab[((int64_t)j * layers + layer) * 2];
-        vp[u] = tab[((int64_t)j * layers + layer) * 2 + 1];
-      }
+  for (int c0 = 0; c0 < n; c0 += kChunk) {
+    const int cn = min(kChunk, n - c0);
+    __syncthreads();                                 // the previous chunk's ids are consumed
+    for (int i = threadIdx.x; i < 2 * cn; i += blockDim.x) {
+      const int j = c0 + (i >> 1);
+      s_ids[i >> 1][i & 1] = tab[((int64_t)j * layers + layer) * 2 + (i & 1)];
     }
-    float kv[kBatch][VPL], vv[kBatch][VPL];
+    __syncthreads();
+    for (int j0 = warp; j0 < cn; j0 += kWarps * kBatch) {
+      // chunk tokens j0, j0 + 4, ..., j0 + 4 (kBatch - 1) of this warp: slices, then the math
+      bool ok[kBatch];
+      int32_t kp[kBatch], vp[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kWarps;
-      ok[u] = kp[u] >= 0 && kp[u] < num_pages && vp[u] >= 0 && vp[u] < num_pages;   // same in every lane
-      if (j < n && !ok[u] && lane == 0) flag_error(err, LORA_DEV_BAD_PAGE);
-      if (ok[u]) {
-        load_slice<VPL>(pool + (int64_t)kp[u] * H + col, kv[u]);
-        load_slice<VPL>(pool + (int64_t)vp[u] * H + col, vv[u]);
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kWarps;
+        kp[u] = vp[u] = -1;
+        if (j < cn) {
+          kp[u] = s_ids[j][0];
+          vp[u] = s_ids[j][1];
+        }
       }
-    }
+      float kv[kBatch][VPL], vv[kBatch][VPL];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (!ok[u]) continue;
-      float s = 0.f;
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kWarps;
+        ok[u] = kp[u] >= 0 && kp[u] < num_pages && vp[u] >= 0 && vp[u] < num_pages;   // same in every lane
+        if (j < cn && !ok[u] && lane == 0) flag_error(err, LORA_DEV_BAD_PAGE);
+        if (ok[u]) {
+          load_slice<VPL>(pool + (int64_t)kp[u] * H + col, kv[u]);
+          load_slice<VPL>(pool + (int64_t)vp[u] * H + col, vv[u]);
+        }
+      }
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) s = fmaf(qv[i], kv[u][i], s);
+      for (int u = 0; u < kBatch; ++u) {
+        if (!ok[u]) continue;
+        float s = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      s *= scale;
-      const float m_new = fmaxf(m, s);
-      const float c = expf(m - m_new);             // 0 on the first token (m = -inf)
-      const float pj = expf(s - m_new);
-      l = l * c + pj;
+        for (int i = 0; i < VPL; ++i) s = fmaf(qv[i], kv[u][i], s);
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) acc[i] = fmaf(pj, vv[u][i], acc[i] * c);
-      m = m_new;
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        s *= scale;
+        const float m_new = fmaxf(m, s);
+        const float c = expf(m - m_new);             // 0 on the first token (m = -inf)
+        const float pj = expf(s - m_new);
+        l = l * c + pj;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) acc[i] = fmaf(pj, vv[u][i], acc[i] * c);
+        m = m_new;
+      }
     }
   }
   if (lane == 0) {

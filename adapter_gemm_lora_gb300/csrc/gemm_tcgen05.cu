@@ -327,11 +327,11 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 
 // ---- persistent variant (batches of more than 256 tokens) ---------------------------------
 // One launch serves the n (1 .. LORA_MAX_GROUP) slots of a call that read the same x (q, k and v
-// of a layer, or a single slot).  Its tiles are (slot, token tile, feature tile) triples, slot
-// major; each CTA walks the tiles c, c + gridDim.x, ...  Consecutive tiles are consecutive
-// feature tiles of one token tile, so the CTAs of a wave share x tiles in L2, and a slot's W
-// stays in L2 while its tiles are in flight.  TMEM holds two accumulators of BN columns.  Warp 0
-// issues TMA loads without pause across tile boundaries, warp 1 issues the MMAs of tile i into
+// of a layer, or a single slot).  Its tiles are (slot, feature tile, token tile) triples, slot
+// major; each CTA walks the tiles c, c + gridDim.x, ...  Within a slot the tiles run in the order
+// tile_m / tile_t give, which keeps the smaller of x and W in L2 across waves.  TMEM holds two
+// accumulators of BN columns.  Warp 0 issues TMA loads without pause across tile boundaries,
+// warp 1 issues the MMAs of tile i into
 // accumulator i % 2, and warps 4-7 (one per TMEM lane quarter) drain accumulator (i-1) % 2
 // meanwhile: add the delta (read straight from global memory), round to bf16, store y from
 // registers.  So a tile's epilogue runs under the next tile's main loop, and one launch for a
@@ -356,6 +356,7 @@ struct PersistParams {
   int32_t m_tiles, t_tiles;        // feature tiles; token tiles (per slot)
   int32_t n_ctiles;                // n_group * m_tiles * t_tiles
   int32_t n_group;
+  int32_t t_inner;                 // order of a slot's tiles: token tile fastest (see tile_m)
   uint16_t* y[LORA_MAX_GROUP];
   const float* delta[LORA_MAX_GROUP];
   int32_t slot[LORA_MAX_GROUP];
@@ -367,6 +368,14 @@ struct PersistParams {
   int32_t lora_only;               // 1: the LoRA extension alone, fp32 into dbg, fused tiles only
   float* dbg[LORA_MAX_GROUP];
 };
+
+// A slot's tile r is (feature tile, token tile).  Consecutive tiles run in one wave of CTAs, so the
+// operand whose tiles change fastest is re-read by every wave: with the token tile fastest
+// (t_inner, batches of fewer tokens than features) x is re-read and each W tile is taken by all
+// token tiles of a wave, so W crosses DRAM once; otherwise W is re-read and x crosses once.  The
+// operand re-read is the smaller one, which stays in L2.
+__device__ __forceinline__ int tile_m(const PersistParams& pp, int r) { return pp.t_inner ? r / pp.t_tiles : r % pp.m_tiles; }
+__device__ __forceinline__ int tile_t(const PersistParams& pp, int r) { return pp.t_inner ? r % pp.t_tiles : r / pp.m_tiles; }
 
 // The LoRA extension of one tile on one slot: -1 when the tile is not fused, else the number of
 // the tile's adapters that carry LoRA on the slot, with their page-table rows and ranks.
@@ -469,8 +478,8 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       bool ok = true, waited = false;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
-        const int m0 = (r % pp.m_tiles) * BM;
-        const int tt = r / pp.m_tiles;
+        const int m0 = tile_m(pp, r) * BM;
+        const int tt = tile_t(pp, r);
         const int t0 = tt * p.BN;
         const CUtensorMap* tw = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
         const CUtensorMap* ts = g == 0 ? &tm_s0 : g == 1 ? &tm_s1 : g == 2 ? &tm_s2 : &tm_s3;
@@ -523,7 +532,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       bool ok = true, waited = false;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
-        const int tt = r / pp.m_tiles;
+        const int tt = tile_t(pp, r);
         TileLora TL;
         TL.nb = -1;
         if (pp.lora_only) {
@@ -606,8 +615,8 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       bool ok = true;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
-        const int m0 = (r % pp.m_tiles) * BM;
-        const int tt = r / pp.m_tiles;
+        const int m0 = tile_m(pp, r) * BM;
+        const int tt = tile_t(pp, r);
         TileLora TL;
         tile_lora(pp, p, tt, slot_of(pp, g), TL);
         it += nk;
@@ -662,13 +671,13 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     int tile = 0;
     for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas) {
       const int g = ct / per_slot, r = ct % per_slot;
-      const int m0 = (r % pp.m_tiles) * BM;
-      const int t0 = (r / pp.m_tiles) * p.BN;
+      const int m0 = tile_m(pp, r) * BM;
+      const int t0 = tile_t(pp, r) * p.BN;
       const int feat = m0 + row;
       const int slot = slot_of(pp, g);
       TileLora TL;
       TL.nb = -1;
-      if (fused_mode) tile_lora(pp, p, r / pp.m_tiles, slot, TL);
+      if (fused_mode) tile_lora(pp, p, tile_t(pp, r), slot, TL);
       if (pp.lora_only && TL.nb < 0) continue;
       const int b = tile & 1;
       const uint32_t tph = (tile >> 1) & 1;
@@ -1098,6 +1107,7 @@ int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_
   pp.m_tiles = g.m_tiles;
   pp.t_tiles = g.n_tiles;
   pp.n_group = n;
+  pp.t_inner = T < H ? 1 : 0;                           // x smaller than W: keep x in L2
   pp.n_ctiles = n * g.m_tiles * g.n_tiles;
   for (int i = 0; i < LORA_MAX_GROUP; ++i) {
     const int j = i < n ? i : 0;

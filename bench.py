@@ -226,14 +226,22 @@ def gemm_kernel_name(H, T, n_sm):
 
 
 # ------------------------------------------------------------------------------- our arm
+def stack_layers(layers):
+    """Spec overrides that cut the layer stack to its first `layers` layers (the same batch, adapters
+    and ranks; a pool scaled to the layers' pages): every projection launch is the full stack's."""
+    spec = workloads.SPECS[5]
+    return {"layers": layers, "n_slots": 4 * layers,
+            "pool_pages": -(-spec.pool_pages * layers // spec.layers)}
+
+
 class Harness:
-    def __init__(self, key, device):
+    def __init__(self, key, device, overrides=None):
         import torch
         import adapter_gemm_lora_gb300 as L
         from adapter_gemm_lora_gb300 import build as B
         B.build()
         self.L, self.torch = L, torch
-        self.wl = wl = workloads.make(key)
+        self.wl = wl = workloads.make(key, **(overrides or {}))
         self.key = key
         H, S, T = wl.H, wl.n_slots, wl.T
         self.dev = device
@@ -537,7 +545,8 @@ def run_ours(args):
     device = torch.device("cuda", local)
     key = args.config
     steps = args.steps if args.steps is not None else default_steps(key)
-    h = Harness(key, device)
+    overrides = stack_layers(args.layers) if key == 5 and args.layers else None
+    h = Harness(key, device, overrides)
     wl = h.wl
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = visible.split(",")[local] if visible else str(local)
@@ -610,7 +619,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights and adapters)",
         "config": {"workload": wl.spec.name, "description": wl.spec.description, "H": wl.H, "T": T,
-                   "slots": wl.n_slots, "adapters_resident": wl.spec.n_adapters,
+                   "slots": wl.n_slots, "layers": wl.spec.layers, "adapters_resident": wl.spec.n_adapters,
                    "distinct_adapters_in_batch": alg["distinct_adapters"], "pool_pages": wl.spec.pool_pages,
                    "parallelism": f"replicas x{world}",
                    "l2": ("flushed (256 MB write) before every step" if h.flush else
@@ -781,6 +790,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-attention", action="store_true", help="skip the paged decode attention leg")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer stack only: keep its first N layers (profiling a stack-shaped step)")
     ap.add_argument("--prefetch", action="store_true",
                     help="also measure decode steps with adapter loads on a copy stream")
     args = ap.parse_args(argv)
