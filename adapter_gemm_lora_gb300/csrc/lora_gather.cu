@@ -8,20 +8,21 @@
 //   expand  delta[t, n] = sum_j s[t, j] * B[j, n]        (B page j = row j of B, H values)
 //
 // Work unit: up to 16 tokens of one segment (tokens that share an adapter), handled by a
-// cluster of 4 CTAs.  One launch may serve several projection slots that read the same x
-// (q, k and v of a layer): its work items are then every unit once per slot, each with its
-// slot's page table and delta buffer, so the short per-slot work lists of a decode batch
-// become one list long enough to keep every cluster busy.  CTA q owns one quarter of the feature range, [q H/4, (q+1) H/4), for
-// both products: it reads that quarter of the unit's token rows of x, of all r A pages and of
-// all r B pages, and nothing else.  The shrink over its quarter gives partial sums of s; the
-// four partials are exchanged through distributed shared memory and added in a fixed order,
-// so every CTA holds the same complete s.  The expand then writes the CTA's quarter of delta.
+// cluster of KC CTAs (KC = 2 for H <= 2048, else 4).
+// One launch may serve several projection slots that read the same x (q, k and v of a layer):
+// its work items are then every unit once per slot, each with its slot's page table and delta
+// buffer, so the short per-slot work lists of a decode batch become one list long enough to keep
+// every cluster busy.  CTA q owns one share of the feature range, [q H/KC, (q+1) H/KC), for both
+// products: it reads that share of the unit's token rows of x, of all r A pages and of all r B
+// pages, and nothing else.  The shrink over its share gives partial sums of s; the KC partials
+// are exchanged through distributed shared memory and added in cluster-rank order, so every CTA
+// holds the same complete s.  The expand then writes the CTA's share of delta.
 //
-// Data movement: one producer warp streams page-row slices (at most 1024 features, 2 KB) into a
-// ring of 5 shared-memory stages with TMA bulk copies (cp.async.bulk), 16 rows per stage:
-// the x rows of the unit, then the A pages 16 at a time, then the B pages 16 at a time.  Up to
-// 160 KB per SM is in flight, so the page gather runs at memory speed without register
-// staging.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
+// Data movement: one producer warp streams page-row slices (at most 1024 features, 2 KB) with
+// TMA bulk copies (cp.async.bulk): the unit's x rows into a buffer of their own, held across the
+// shrink, and the A pages, then the B pages, into a ring of 2 stages of 32 rows (two groups of 16
+// rank columns), each lane copying one row.  Up to 64 page rows and 16 x rows are in flight per
+// SM, without register staging.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
 // level bf16 MMA (m16n8k16, fp32 accumulation), feeding operands with ldmatrix straight from
 // the staged page rows: a unit holds 16 tokens at most, below the 64-row minimum tile of the
 // asynchronous tcgen05 MMA, while ldmatrix takes any row addresses, which is what a page
@@ -39,7 +40,6 @@
 
 namespace {
 
-constexpr int kCluster = 4;                    // CTAs per unit, one feature quarter each
 constexpr int kUnitTok = kUnitTokens;         // tokens per unit (16)
 constexpr int kFB = 1024;                      // features per stage row (one feature block)
 constexpr int kRows = 32;                      // page rows per ring stage: two groups of 16
@@ -57,13 +57,17 @@ constexpr int kSbPitch = LORA_MAX_RANK + 8;    // bf16 elements per token row of
 constexpr int kOffRing = 0;
 constexpr int kOffX = kOffRing + kStages * kSlotBytes;                       // [16 tokens][kRowBytes]
 constexpr int kOffPart = kOffX + kXRows * kRowBytes;                         // [8 warps][16][16] f32
-constexpr int kOffExch = kOffPart + kConsumerWarps * 16 * 16 * 4;            // [2][4][64][16] f32
-constexpr int kOffSb = kOffExch + 2 * kCluster * LORA_MAX_RANK * kUnitTok * 4;  // [2][16][kSbPitch] bf16
-constexpr int kOffBar = kOffSb + 2 * kUnitTok * kSbPitch * 2;
-constexpr int kSmemBytes = kOffBar + (2 * kStages + 4) * 8;
 static_assert(kUnitTok == 16, "the MMA tiling assumes 16 tokens per unit");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kOffSb % 16 == 0 && kOffBar % 8 == 0, "alignment");
+// The rest of the layout depends on the number KC of CTAs that split an item's features.
+template <int KC>
+struct Smem {
+  static constexpr int kOffExch = kOffPart + kConsumerWarps * 16 * 16 * 4;                 // [2][KC][64][16] f32
+  static constexpr int kOffSb = kOffExch + 2 * KC * LORA_MAX_RANK * kUnitTok * 4;          // [2][16][kSbPitch] bf16
+  static constexpr int kOffBar = kOffSb + 2 * kUnitTok * kSbPitch * 2;
+  static constexpr int kBytes = kOffBar + (2 * kStages + 4) * 8;
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kOffSb % 16 == 0 && kOffBar % 8 == 0, "alignment");
+};
 
 __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
   atomicCAS(err, 0, LORA_EDEVICE);
@@ -226,16 +230,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_
                : "memory");
 }
 
+template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
 lora_delta_kernel(LoraLaunch L, lora_segments seg) {
+  constexpr int kCluster = KC;                            // CTAs per item, one feature share each
+  using SM = Smem<KC>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t q = cluster_rank();
   const uint32_t ring = smem_u32(smem + kOffRing);
   float* part = reinterpret_cast<float*>(smem + kOffPart);
-  float* exch = reinterpret_cast<float*>(smem + kOffExch);
-  __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smem + kOffSb);
-  const uint32_t bar_full = smem_u32(smem + kOffBar);
+  float* exch = reinterpret_cast<float*>(smem + SM::kOffExch);
+  __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smem + SM::kOffSb);
+  const uint32_t bar_full = smem_u32(smem + SM::kOffBar);
   const uint32_t bar_empty = bar_full + 8 * kStages;
   const uint32_t bar_exch = bar_empty + 8 * kStages;
   const uint32_t bar_xfull = bar_exch + 16, bar_xempty = bar_xfull + 8;
@@ -425,12 +432,13 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
         }
         ok = ok && wait_warp(bar_exch + 8 * b, (n_done >> 1) & 1);
         ++n_done;
-        // s = sum of the four quarters (fixed order), split into bf16 hi + lo, token-major
+        // s = sum of the KC shares in cluster-rank order, split into bf16 hi + lo, token-major
         for (int e = tid; e < ng * 256; e += kConsumers) {
           const int j = e >> 4, t = e & 15;
           const float* ex = exch + (b * kCluster * LORA_MAX_RANK + j) * kUnitTok + t;
-          const float v = ((ex[0] + ex[LORA_MAX_RANK * kUnitTok]) + ex[2 * LORA_MAX_RANK * kUnitTok]) +
-                          ex[3 * LORA_MAX_RANK * kUnitTok];
+          float v = ex[0];
+#pragma unroll
+          for (int c = 1; c < kCluster; ++c) v += ex[c * LORA_MAX_RANK * kUnitTok];
           const __nv_bfloat16 hi = __float2bfloat16_rn(v);
           sb_hi[t * kSbPitch + j] = hi;
           sb_lo[t * kSbPitch + j] = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -506,57 +514,69 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   cluster_sync_all();                                     // no CTA leaves while a peer may still address it
 }
 
+template <int KC>
 int active_clusters() {
-  static int cached[64] = {0};
+  static int cached[kMaxDeviceFlags] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] > 0) return cached[dev];
+  const bool cache = dev >= 0 && dev < kMaxDeviceFlags;
+  if (cache && cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCluster * 64);
+  cfg.gridDim = dim3(KC * 64);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Smem<KC>::kBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.x = KC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, lora_delta_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, lora_delta_kernel<KC>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    n = device_sm_count() / kCluster;
+    n = device_sm_count() / KC;
   }
-  cached[dev] = n;
+  if (cache) cached[dev] = n;
   return n;
 }
 
-}  // namespace
-
-int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
+template <int KC>
+int launch_delta_kc(const LoraLaunch& L, cudaStream_t st) {
   static DeviceFlags attr;
-  int rc = ensure_smem_attr(attr, lora_delta_kernel, kSmemBytes, "lora_delta_kernel: shared memory attribute");
+  int rc = ensure_smem_attr(attr, lora_delta_kernel<KC>, Smem<KC>::kBytes, "lora_delta_kernel: shared memory attribute");
   if (rc != LORA_OK) return rc;
   // Persistent clusters, as many as can be resident; each loops over the units.
-  int groups = active_clusters();
+  int groups = active_clusters<KC>();
   const int item_cap = L.seg->unit_cap * L.n_group;
   if (item_cap < groups) groups = item_cap > 0 ? item_cap : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(groups * kCluster);
+  cfg.gridDim = dim3(groups * KC);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Smem<KC>::kBytes;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = kCluster;
+  attrs[0].val.clusterDim.x = KC;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = L.pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_delta_kernel, L, *L.seg);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_delta_kernel<KC>, L, *L.seg);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "lora_delta_kernel launch");
+}
+
+}  // namespace
+
+// The feature split of an item: 2 CTAs when their halves are at most 1024 features (H <= 2048:
+// twice as many items run at once), else 4.  A split into 5 (H = 5120: one 2 KB slice per page
+// row instead of a 2 KB and a 512 B one) made the kernel alone faster but a layer's chain of
+// kernels slower: its 150 SMs leave no room for the next kernel to start early.
+int delta_split(int32_t H) { return H <= 2048 ? 2 : 4; }
+
+int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
+  return delta_split(L.H) == 2 ? launch_delta_kc<2>(L, st) : launch_delta_kc<4>(L, st);
 }
