@@ -448,7 +448,8 @@ def attention_leg(L, H, device, n_req=256, ctx=(128, 2048), head_dim=128, calls=
         nbytes = int(2 * lens.sum()) * H * 2 + 2 * n_req * H * 2
         peaks = load_peaks()
         gbs = nbytes / (us * 1e-6) / 1e9
-        return {"kernel": "attention_decode_kernel", "requests": n_req, "H": H, "head_dim": head_dim,
+        kernel = "attention_heads_kernel"
+        return {"kernel": kernel, "requests": n_req, "H": H, "head_dim": head_dim,
                 "context": f"uniform [{ctx[0]}, {ctx[1]}], mean {lens.mean():.0f}", "us_per_call": round(us, 2),
                 "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                 "frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm"}

@@ -52,6 +52,11 @@ def _scene(L, H, layers, lengths, seed):
     (256, 2, 2, [1, 5, 0, 33, 7]),        # D = 128, an empty request, ragged lengths
     (512, 8, 1, [64, 3, 17]),            # D = 64
     (1024, 8, 3, [129, 1, 40, 2, 96, 11]),
+    (2048, 16, 1, [300, 0, 1, 77]),       # two head groups
+    (4096, 64, 2, [50, 3, 200]),          # D = 64, eight head groups
+    (8192, 64, 1, [40, 7, 129]),          # D = 128, eight head groups
+    (8192, 128, 1, [33, 5]),              # D = 64, sixteen head groups
+    (640, 5, 1, [17, 9, 24]),             # a group of five heads: three warps idle
 ])
 def test_attention_decode_matches_oracle(L, H, n_heads, layers, lengths):
     import torch
@@ -77,23 +82,24 @@ def test_attention_decode_matches_oracle(L, H, n_heads, layers, lengths):
         L.lora_pool_destroy(pool)
 
 
-def test_attention_decode_bad_page_sets_the_error_word(L):
+@pytest.mark.parametrize("H,n_heads", [(256, 2), (8192, 128)])
+def test_attention_decode_bad_page_sets_the_error_word(L, H, n_heads):
     import torch
-    pool, pool_t, model, opool, rng = _scene(L, 256, 1, [4], seed=5)
+    pool, pool_t, model, opool, rng = _scene(L, H, 1, [4], seed=5)
     table = torch.empty((1, 4, 1, 2), dtype=torch.int32, device="cuda")
     seq = torch.empty(1, dtype=torch.int32, device="cuda")
     try:
         L.lora_kv_batch_table(pool, [100], 4, table, seq)
         table[0, 2, 0, 0] = 1 << 30                        # a page id outside the pool: skipped, reported
-        q_bits = workloads.to_bf16_bits(rng.standard_normal((1, 256)).astype(np.float32))
-        out = torch.empty((1, 256), dtype=torch.bfloat16, device="cuda")
-        L.lora_attention_decode(pool, 1, table, seq, 4, 1, 0, bits_to_torch(q_bits), out, 2)
+        q_bits = workloads.to_bf16_bits(rng.standard_normal((1, H)).astype(np.float32))
+        out = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+        L.lora_attention_decode(pool, 1, table, seq, 4, 1, 0, bits_to_torch(q_bits), out, n_heads)
         torch.cuda.synchronize()
         with pytest.raises(L.LoraError) as e:
             L.lora_status(pool)
         assert e.value.code == L.LORA_EDEVICE
         tab = model.kv_table(100, 0)
-        want = O.attention_decode(opool, [tab[[0, 1, 3]]], q_bits, 2)     # the bad token left out
+        want = O.attention_decode(opool, [tab[[0, 1, 3]]], q_bits, n_heads)     # the bad token left out
         got = O.bf16_to_f64(torch_to_bits(out))
         assert np.all(np.abs(got - want) <= 1e-2 * (1 + np.abs(want)))
     finally:
