@@ -352,6 +352,15 @@ gemm_lora_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 // A operand).  The epilogue of a fused tile adds no delta: y = bf16(acc), rounded once.  A
 // LoRA-only launch (for delta_dbg) runs the extension alone on the fused tiles and writes the
 // fp32 accumulator to the debug buffer.
+//
+// MH = 2: tiles of 256 features.  Each K step issues two M = 128 MMAs that share the stage's x
+// tile, into two accumulators of BN columns (all 512 TMEM columns, so one tile at a time: the
+// epilogue, now 8 warps, two per lane quarter, is no longer hidden under the next tile), and a
+// stage holds 256 W rows.  The shared-memory fill per flop drops by a third (W 32 KB + x 32 KB
+// per 64-wide K block for 2 x 128 x 256 x 64 MACs, against 16 + 32 KB for half of them), which
+// is what bounds the 128-feature tiles of a prefill-shaped batch.  The LoRA extension gathers
+// B rows for both 128-feature blocks of the tile into the stage's W area, one block after the
+// other.
 struct PersistParams {
   int32_t m_tiles, t_tiles;        // feature tiles; token tiles (per slot)
   int32_t n_ctiles;                // n_group * m_tiles * t_tiles
@@ -414,7 +423,8 @@ __device__ __forceinline__ int slot_of(const PersistParams& pp, int g) {
 }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__global__ void __launch_bounds__(THREADS, 1)
+template <int MH>
+__global__ void __launch_bounds__(THREADS + (MH - 1) * 128, 1)
 gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_w3,
                      const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_s0,
@@ -435,13 +445,17 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
   // theirs on the empty barrier could be several phases behind and pass or block wrongly.)
   const uint32_t bar_go = bar_wl + 8 * MAX_STAGES;
 
+  constexpr int TM = MH * BM;                           // features per tile
+  constexpr int N_EPI = 4 * MH;                         // epilogue warps
+  constexpr int N_ACC = 3 - MH;                         // accumulator buffers (one per tile in flight)
+  constexpr uint32_t WB = (uint32_t)MH * A_BYTES;       // W rows of one K chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int stages = p.stages;
   const int kc = p.kc;
   const uint32_t xb = (uint32_t)(p.BN * BK * 2);
-  const uint32_t stage_bytes = (uint32_t)kc * (A_BYTES + xb);
+  const uint32_t stage_bytes = (uint32_t)kc * (WB + xb);
   const int nk = pp.lora_only ? 0 : p.n_kb / kc;         // base stages per tile
-  const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator
+  const uint32_t acc_cols = tmem_cols_for(p.BN);        // one accumulator (MH = 2: one half of the tile)
   const int n_ctas = (int)gridDim.x;
   const int per_slot = pp.m_tiles * pp.t_tiles;
   const bool fused_mode = pp.tile_plan != nullptr;
@@ -455,7 +469,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, 4);                 // one arrival per epilogue warp
+      mbar_init(bar_tempty + 8 * b, N_EPI);             // one arrival per epilogue warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
@@ -478,7 +492,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       bool ok = true, waited = false;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
-        const int m0 = tile_m(pp, r) * BM;
+        const int m0 = tile_m(pp, r) * TM;
         const int tt = tile_t(pp, r);
         const int t0 = tt * p.BN;
         const CUtensorMap* tw = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
@@ -495,8 +509,10 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           const uint32_t st = s_base + (uint32_t)s * stage_bytes;
           for (int c = 0; c < kc; ++c) {
             const int kx = (i * kc + c) * BK;
-            tma_load_2d(st + (uint32_t)c * A_BYTES, tw, kx, m0, bar_full + 8 * s, pol_w);
-            tma_load_2d(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              tma_load_2d(st + (uint32_t)c * WB + (uint32_t)h * A_BYTES, tw, kx, m0 + h * BM, bar_full + 8 * s, pol_w);
+            tma_load_2d(st + (uint32_t)kc * WB + (uint32_t)c * xb, &tm_x, kx, t0, bar_full + 8 * s, pol_x);
           }
         }
         if (!ok || !fused_mode) continue;
@@ -516,7 +532,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
             }
             if (part == 0) mbar_arrive(bar_go + 8 * s);     // the loaders may write this slot's B rows
             mbar_arrive_expect_tx(bar_full + 8 * s, xb);
-            tma_load_2d(s_base + (uint32_t)s * stage_bytes + A_BYTES, ts,
+            tma_load_2d(s_base + (uint32_t)s * stage_bytes + WB, ts,
                         TL.tmap_b[b] * 2 * LORA_MAX_RANK + part * LORA_MAX_RANK, t0, bar_full + 8 * s, pol_x);
           }
         }
@@ -543,14 +559,14 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           tile_lora(pp, p, tt, slot_of(pp, g), TL);
           if (TL.nb < 0) continue;                        // the LoRA-only pass skips unfused tiles
         }
-        const int b = tile & 1;
-        if (!mbar_wait(bar_tempty + 8 * b, ((tile >> 1) & 1) ^ 1)) {   // accumulator b drained
+        const int b = tile % N_ACC;
+        if (!mbar_wait(bar_tempty + 8 * b, ((tile / N_ACC) & 1) ^ 1)) {   // accumulator b drained
           flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
           break;
         }
         ++tile;
         tc_fence_after();
-        const uint32_t acc = tmem + (uint32_t)b * acc_cols;
+        const uint32_t acc = tmem + (uint32_t)b * acc_cols;   // MH = 2: b = 0, halves at acc and acc + acc_cols
         for (int i = 0; i < nk; ++i, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1;
@@ -562,11 +578,14 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           tc_fence_after();
           const uint32_t st = s_base + (uint32_t)s * stage_bytes;
           for (int c = 0; c < kc; ++c) {
-            const uint64_t ad = sw128_kmajor_desc(st + (uint32_t)c * A_BYTES);
-            const uint64_t bd = sw128_kmajor_desc(st + (uint32_t)kc * A_BYTES + (uint32_t)c * xb);
+            const uint64_t bd = sw128_kmajor_desc(st + (uint32_t)kc * WB + (uint32_t)c * xb);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              mma_bf16_ss(acc, ad + 2 * k, bd + 2 * k, idesc, (i | c | k) != 0);
+#pragma unroll
+              for (int h = 0; h < MH; ++h)
+                mma_bf16_ss(acc + (uint32_t)h * acc_cols,
+                            sw128_kmajor_desc(st + (uint32_t)c * WB + (uint32_t)h * A_BYTES) + 2 * k, bd + 2 * k,
+                            idesc, (i | c | k) != 0);
           }
           mma_commit(bar_empty + 8 * s);
         }
@@ -591,13 +610,16 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           }
           tc_fence_after();
           const uint32_t st0 = s_base + (uint32_t)s0 * stage_bytes, st1 = s_base + (uint32_t)s1 * stage_bytes;
-          const uint64_t bh = sw128_kmajor_desc(st0 + A_BYTES), bl = sw128_kmajor_desc(st1 + A_BYTES);
+          const uint64_t bh = sw128_kmajor_desc(st0 + WB), bl = sw128_kmajor_desc(st1 + WB);
           const int n16 = (TL.r[lb] + 15) / 16;
           for (int k = 0; k < n16; ++k) {                 // 16 rank columns: two 8-row groups of B
-            const uint64_t ad = sw128_mnmajor_desc(st0 + (uint32_t)k * 4096u, 1024u, 2048u);
-            mma_bf16_ss(acc, ad, bh + 2 * k, idesc_mn, first ? 0u : 1u);
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {                // B rows of feature block h at h x A_BYTES
+              const uint64_t ad = sw128_mnmajor_desc(st0 + (uint32_t)h * A_BYTES + (uint32_t)k * 4096u, 1024u, 2048u);
+              mma_bf16_ss(acc + (uint32_t)h * acc_cols, ad, bh + 2 * k, idesc_mn, first ? 0u : 1u);
+              mma_bf16_ss(acc + (uint32_t)h * acc_cols, ad, bl + 2 * k, idesc_mn, 1u);
+            }
             first = false;
-            mma_bf16_ss(acc, ad, bl + 2 * k, idesc_mn, 1u);
           }
           mma_commit(bar_empty + 8 * s0);
           mma_commit(bar_empty + 8 * s1);
@@ -615,26 +637,25 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       bool ok = true;
       for (int ct = (int)blockIdx.x; ct < pp.n_ctiles && ok; ct += n_ctas) {
         const int g = ct / per_slot, r = ct % per_slot;
-        const int m0 = tile_m(pp, r) * BM;
+        const int m0 = tile_m(pp, r) * TM;
         const int tt = tile_t(pp, r);
         TileLora TL;
         tile_lora(pp, p, tt, slot_of(pp, g), TL);
         it += nk;
         for (int lb = 0; lb < TL.nb && ok; ++lb, it += 2) {
-          // chunk c = l + 64 i: row j = c / 16 (rank column), 64-feature half h = (c / 8) % 2,
-          // 16-byte piece c % 8; page ids are read before the stage is free
+          // chunk c = l + 64 i of a 128-feature block: row j = c / 16 (rank column), 64-feature
+          // half h = (c / 8) % 2, 16-byte piece c % 8; page ids are read before the stage is free
           const int r16 = (TL.r[lb] + 15) & ~15;
-          int64_t src[16];
+          int64_t src[16];                                // the page row's start; -1: zero
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = l + 64 * i;
-            const int j = c >> 4, h = (c >> 3) & 1, piece = c & 7;
-            const int f = m0 + h * 64 + piece * 8;
-            src[i] = -1;                                  // zero: past the rank, past H or a bad page
-            if (c < r16 * 16 && j < TL.r[lb] && f < p.H) {
+            const int j = c >> 4;
+            src[i] = -1;                                  // zero: past the rank or a bad page
+            if (c < r16 * 16 && j < TL.r[lb]) {
               const int64_t page = __ldg(TL.tab[lb] + LORA_MAX_RANK + j);
               if (page >= 0 && page < pp.num_pages)
-                src[i] = page * p.H + f;
+                src[i] = page * p.H;
               else
                 flag_error(p.err, LORA_DEV_BAD_PAGE);
             }
@@ -646,14 +667,19 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           if (!ok) break;
           const uint32_t st = s_base + (uint32_t)s * stage_bytes;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = l + 64 * i;
-            if (c < r16 * 16) {
-              const int j = c >> 4, h = (c >> 3) & 1, piece = c & 7;
-              cp_async_16(st + (uint32_t)(j >> 3) * 2048u + (uint32_t)h * 1024u + sw128_offset(j, piece),
-                          pp.pool + (src[i] >= 0 ? src[i] : 0), src[i] >= 0);
+          for (int blk = 0; blk < MH; ++blk)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = l + 64 * i;
+              if (c < r16 * 16) {
+                const int j = c >> 4, h = (c >> 3) & 1, piece = c & 7;
+                const int f = m0 + blk * BM + h * 64 + piece * 8;
+                const bool valid = src[i] >= 0 && f < p.H;          // zero past H
+                cp_async_16(st + (uint32_t)blk * A_BYTES + (uint32_t)(j >> 3) * 2048u + (uint32_t)h * 1024u +
+                                sw128_offset(j, piece),
+                            pp.pool + (valid ? src[i] + f : 0), valid);
+              }
             }
-          }
           cp_async_commit();
           cp_async_wait<0>();
           fence_proxy_async_shared();
@@ -664,14 +690,14 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       if (!ok && lane == 0) flag_error(p.err, LORA_DEV_WAIT_TIMEOUT);
     }
   } else {
-    // ---- epilogue warps: TMEM lane quarter q = warp - 4 ----
-    const int q = warp - 4;
-    const int row = q * 32 + lane;
+    // ---- epilogue warps: TMEM lane quarter q = warp % 4 of feature block hf ----
+    const int q = (warp - 4) & 3, hf = (warp - 4) >> 2;
+    const int row = hf * BM + q * 32 + lane;
     pdl_wait_then_release();                            // delta, ids and the plan come from earlier kernels
     int tile = 0;
     for (int ct = (int)blockIdx.x; ct < pp.n_ctiles; ct += n_ctas) {
       const int g = ct / per_slot, r = ct % per_slot;
-      const int m0 = tile_m(pp, r) * BM;
+      const int m0 = tile_m(pp, r) * TM;
       const int t0 = tile_t(pp, r) * p.BN;
       const int feat = m0 + row;
       const int slot = slot_of(pp, g);
@@ -679,8 +705,8 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       TL.nb = -1;
       if (fused_mode) tile_lora(pp, p, tile_t(pp, r), slot, TL);
       if (pp.lora_only && TL.nb < 0) continue;
-      const int b = tile & 1;
-      const uint32_t tph = (tile >> 1) & 1;
+      const int b = tile % N_ACC;
+      const uint32_t tph = (tile / N_ACC) & 1;
       ++tile;
       uint16_t* y = pp.y[0];
       const float* delta = pp.delta[0];
@@ -699,7 +725,7 @@ gemm_lora_persistent(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
         break;
       }
       tc_fence_after();
-      const uint32_t acc_row = tmem + (uint32_t)b * acc_cols + ((uint32_t)(q * 32) << 16);
+      const uint32_t acc_row = tmem + (uint32_t)(b + hf) * acc_cols + ((uint32_t)(q * 32) << 16);
       const int n_chunks = p.BN / 32;
       for (int c4 = 0; c4 < n_chunks; c4 += 4) {
         unsigned pm[4] = {0u, 0u, 0u, 0u};              // a fused tile's LoRA term is in the accumulator
@@ -1003,7 +1029,7 @@ int persistent_ctas() {
   if (dev < 0 || dev >= 64) dev = 0;
   if (cached[dev] > 0) return cached[dev];
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_lora_persistent, THREADS, SMEM_BYTES) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_lora_persistent<1>, THREADS, SMEM_BYTES) != cudaSuccess ||
       per_sm <= 0) {
     cudaGetLastError();
     per_sm = 1;
@@ -1078,14 +1104,34 @@ GemmParams gemm_params(const GemmLaunch& G, const Geometry& g) {
   return P;
 }
 
+// Feature-tile height of a persistent launch: 256-feature tiles (MH = 2) for 256-token tiles when
+// their waves cost less.  A 256-feature tile takes about 1.5 times as long as a 128-feature one
+// (twice the flops at two thirds of the shared-memory fill per flop, its epilogue not hidden), so
+// MH = 2 is taken when 1.5 x its waves is below the waves of 128-feature tiles; a batch whose
+// 256-feature tiles leave the last wave nearly empty keeps 128-feature tiles.
+int persistent_mh(const Geometry& g, int n, int H) {
+  if (g.bn != MAX_BN || g.kc != 1 || g.ks != 1) return 1;
+  const int ctas = persistent_ctas();
+  const int64_t w1 = ((int64_t)n * g.m_tiles * g.n_tiles + ctas - 1) / ctas;
+  const int64_t w2 = ((int64_t)n * ((H + 2 * BM - 1) / (2 * BM)) * g.n_tiles + ctas - 1) / ctas;
+  return 3 * w2 < 2 * w1 ? 2 : 1;
+}
+
 // One persistent launch over the tiles of the n slots G[0..n) (same x, T and H); with `fused`, the
 // plan's fused tiles take their LoRA term in the GEMM (lora_only: that term alone, into lora_dbg).
-int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_t st, bool fused = false,
+int launch_persistent(const GemmLaunch* G, int n, const Geometry& g_in, cudaStream_t st, bool fused = false,
                       bool lora_only = false) {
-  static DeviceFlags attr;
-  int rc = ensure_smem_attr(attr, gemm_lora_persistent, SMEM_BYTES, "gemm kernel attribute");
-  if (rc != LORA_OK) return rc;
   const int H = G[0].H, T = G[0].T;
+  const int mh = persistent_mh(g_in, n, H);
+  Geometry g = g_in;
+  if (mh == 2) {
+    g.m_tiles = (H + 2 * BM - 1) / (2 * BM);
+    g.stages = STAGE_AREA / (2 * A_BYTES + g.bn * BK * 2);
+  }
+  static DeviceFlags attr1, attr2;
+  int rc = mh == 1 ? ensure_smem_attr(attr1, gemm_lora_persistent<1>, SMEM_BYTES, "gemm kernel attribute")
+                   : ensure_smem_attr(attr2, gemm_lora_persistent<2>, SMEM_BYTES, "gemm kernel attribute");
+  if (rc != LORA_OK) return rc;
   CUtensorMap tm_w[LORA_MAX_GROUP], tm_x;
   for (int i = 0; i < n; ++i) {
     rc = encode_2d(&tm_w[i], G[i].W, (uint64_t)H, (uint64_t)H, (uint32_t)BM);
@@ -1125,9 +1171,12 @@ int launch_persistent(const GemmLaunch* G, int n, const Geometry& g, cudaStream_
   }
   int ctas = persistent_ctas();
   if (ctas > pp.n_ctiles) ctas = pp.n_ctiles;
-  cudaError_t e = launch_pdl(G[0].pdl, gemm_lora_persistent, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
-                             tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3],
-                             gemm_params(G[0], g), pp);
+  cudaError_t e =
+      mh == 1 ? launch_pdl(G[0].pdl, gemm_lora_persistent<1>, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
+                           tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3], gemm_params(G[0], g), pp)
+              : launch_pdl(G[0].pdl, gemm_lora_persistent<2>, dim3(ctas), dim3(THREADS + 128), SMEM_BYTES, st,
+                           tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3],
+                           gemm_params(G[0], g), pp);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
 }

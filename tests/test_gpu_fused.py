@@ -96,6 +96,7 @@ FUSED = [
     (2048, [300, 520, 260, 900, 640], 0, [64, 8, 16, 32], [0, 1, 2]),      # group of three slots
     (1024, [1500, 1200, 2000, 640], 300, [16, 64, 8, 40, 3], [0, 1]),     # a decode prefix: unfused tiles too
     (4096, [700, 1000], 0, [64, 16], [0, 1, 2, 3]),                       # group of four, K of 64 blocks
+    (1344, [1500, 2000, 1500], 0, [16, 64, 8], [0, 1, 2]),               # 256-feature tiles, ragged last one
 ]
 
 

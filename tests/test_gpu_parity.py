@@ -131,6 +131,7 @@ GROUP = [
     (384, 100, [8, 64, 5], 3, 0.3, [0, 2, 1]),               # K split over 2 CTAs (6 blocks of 64)
     (4096, 200, [64, 32, 16, 8, 64, 16], 4, 0.1, [0, 1, 2]),  # 96 tiles: several per cluster
     (1024, 2600, [16, 64, 8, 33], 3, 0.2, [0, 1, 2]),         # persistent group vs single-tile launches
+    (1344, 5000, [16, 64, 8], 3, 0.2, [0, 1, 2]),             # 256-feature tiles, the last one 64 features
     (512, 700, [8, 64, 24], 2, 0.25, [1, 0]),                 # persistent group, 32-token tiles, 4 K chunks a stage
     (192, 100, [8, 16, 64], 3, 0.2, [2, 0, 1]),               # K of 3 blocks: no split, persistent group
 ]
