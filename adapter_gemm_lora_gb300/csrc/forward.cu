@@ -73,6 +73,7 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
     G[i].partials_floats = gemm_partial_floats(seg->T_max, H) * cap;
     G[i].err = p->d_err;
     G[i].pdl = !p->prof_on;
+    G[i].prof = p;
     if (seg->tile_plan != nullptr && T > kTileTokens) {
       G[i].tile_plan = seg->tile_plan;
       G[i].s_lora = seg->s_lora + (size_t)i * seg->T_max * kSCols;
@@ -143,20 +144,14 @@ int forward_slots(lora_pool* p, const lora_segments* seg, int32_t n, const int32
         any = any || delta_dbg[i] != nullptr;
       }
       if (any) {
-        ProfScope prof(p, LORA_KIND_GEMM, st);
         rc = launch_gemm_fused(G, n, true, st);
         if (rc != LORA_OK) return rc;
       }
     }
-    ProfScope prof(p, LORA_KIND_GEMM, st);
-    return launch_gemm_fused(G, n, false, st);
+    return launch_gemm_fused(G, n, false, st);       // each GEMM kernel launch is its own profiling scope
   }
-  if (gemm_group_fits(G, n)) {          // decode-sized batch: one launch for every slot of the group
-    ProfScope prof(p, LORA_KIND_GEMM, st);
-    return launch_gemm_group(G, n, st);
-  }
+  if (gemm_group_fits(G, n)) return launch_gemm_group(G, n, st);   // decode-sized batch: one launch for the group
   for (int i = 0; i < n; ++i) {
-    ProfScope prof(p, LORA_KIND_GEMM, st);
     rc = launch_gemm(G[i], st);
     if (rc != LORA_OK) return rc;
   }

@@ -1171,13 +1171,16 @@ int launch_persistent(const GemmLaunch* G, int n, const Geometry& g_in, cudaStre
   }
   int ctas = persistent_ctas();
   if (ctas > pp.n_ctiles) ctas = pp.n_ctiles;
-  cudaError_t e =
-      mh == 1 ? launch_pdl(G[0].pdl, gemm_lora_persistent<1>, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
-                           tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3], gemm_params(G[0], g), pp)
-              : launch_pdl(G[0].pdl, gemm_lora_persistent<2>, dim3(ctas), dim3(THREADS + 128), SMEM_BYTES, st,
-                           tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3],
-                           gemm_params(G[0], g), pp);
-  if (e == cudaSuccess) e = cudaGetLastError();
+  cudaError_t e;
+  {
+    ProfScope prof(G[0].prof, LORA_KIND_GEMM, st);
+    e = mh == 1 ? launch_pdl(G[0].pdl, gemm_lora_persistent<1>, dim3(ctas), dim3(THREADS), SMEM_BYTES, st, tm_w[0],
+                             tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3], gemm_params(G[0], g), pp)
+                : launch_pdl(G[0].pdl, gemm_lora_persistent<2>, dim3(ctas), dim3(THREADS + 128), SMEM_BYTES, st,
+                             tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, tm_s[0], tm_s[1], tm_s[2], tm_s[3],
+                             gemm_params(G[0], g), pp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_persistent launch");
 }
 }  // namespace
@@ -1215,8 +1218,12 @@ int launch_gemm(const GemmLaunch& G, cudaStream_t st) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = G.pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, gemm_params(G, g));
-  if (e == cudaSuccess) e = cudaGetLastError();
+  cudaError_t e;
+  {
+    ProfScope prof(G.prof, LORA_KIND_GEMM, st);
+    e = cudaLaunchKernelEx(&cfg, gemm_lora_kernel, tm_w, tm_x, tm_d, tm_y, gemm_params(G, g));
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_kernel launch");
 }
 
@@ -1322,8 +1329,12 @@ int launch_group_ks(const GemmLaunch* G, int n, const SplitK& sk, cudaStream_t s
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = G[0].pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_lora_group_splitk<KS>, tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, P, gp);
-  if (e == cudaSuccess) e = cudaGetLastError();
+  cudaError_t e;
+  {
+    ProfScope prof(G[0].prof, LORA_KIND_GEMM, st);
+    e = cudaLaunchKernelEx(&cfg, gemm_lora_group_splitk<KS>, tm_w[0], tm_w[1], tm_w[2], tm_w[3], tm_x, P, gp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "gemm_lora_group_splitk launch");
 }
 }  // namespace

@@ -156,6 +156,7 @@ struct GemmLaunch {
   int64_t num_pages;
   const int32_t* rank;
   float* lora_dbg;         // the LoRA-only launch writes the fp32 LoRA term of the fused tiles here
+  const lora_pool* prof;   // each kernel launch is one profiling scope of kind gemm on this pool
 };
 int launch_gemm(const GemmLaunch& G, cudaStream_t st);
 // n (1 .. LORA_MAX_GROUP) slots that read the same x whose batch is cut into 256-token tiles on

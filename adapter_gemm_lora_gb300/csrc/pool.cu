@@ -163,6 +163,7 @@ cudaEvent_t take_event(lora_pool* p) {
 }  // namespace
 
 ProfScope::ProfScope(const lora_pool* pool, int k, cudaStream_t s) : p(const_cast<lora_pool*>(pool)), kind(k), st(s) {
+  if (!p) return;                       // a launch made for no pool (nothing to count)
   p->launches[kind] += 1;
   if (!p->prof_on) return;
   cudaEvent_t a = take_event(p), b = take_event(p);

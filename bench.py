@@ -191,7 +191,8 @@ def algorithmic(wl):
     delta_step = n_groups * t_lora * H * 2 + S * ((lora_pages // S) * H * 2 + t_lora * H * 4)
     delta_bytes = delta_step // n_groups
     return dict(step_bytes=step_bytes, step_flops=step_flops, gemm_bytes=gemm_bytes, gemm_flops=gemm_flops,
-                delta_bytes=delta_bytes,
+                delta_bytes=delta_bytes, gemm_bytes_step=gemm_bytes * len(launches), gemm_flops_step=S * 2 * T * H * H,
+                delta_bytes_step=delta_step,
                 lora_page_bytes=lora_pages * H * 2, distinct_adapters=int(used.size), sum_rank=sum_r)
 
 
@@ -200,21 +201,23 @@ def gemm_kernel_names(wl, n_sm):
     names = []
     for g in gemm_launch_groups(wl):
         split = wl.T <= 256 and (wl.H // 64) % 2 == 0
-        if len(g) > 1:
-            k = f"gemm_lora_group_splitk<{4 if (wl.H // 64) % 4 == 0 else 2}>" if split else "gemm_lora_persistent"
+        if len(g) > 1 and split:
+            ks = [f"gemm_lora_group_splitk<{4 if (wl.H // 64) % 4 == 0 else 2}>"]
         else:
-            k = gemm_kernel_name(wl.H, wl.T, n_sm)
-        if k not in names:
-            names.append(k)
+            ks = gemm_kernel_name(wl.H, wl.T, n_sm, len(g))
+        for k in ks:
+            if k not in names:
+                names.append(k)
     return " + ".join(names)
 
 
-def gemm_kernel_name(H, T, n_sm):
-    """Which base-GEMM kernel the library launches for one slot (its tile choice, restated):
-    batches of <= 256 tokens split K over a cluster; larger ones walk their tiles with
-    persistent CTAs when there are more cluster tiles than clusters fit on the GPU."""
-    if T <= 256:
-        return "gemm_lora_kernel"
+def gemm_kernel_name(H, T, n_sm, n_slots=1):
+    """The base-GEMM kernel the library launches for n_slots slots of T tokens (its tile choice,
+    restated): one slot of <= 256 tokens splits K over a cluster; larger batches walk their tiles
+    with persistent CTAs (one slot: when there are more tiles than SMs), of 256 features
+    (gemm_lora_persistent<2>) when 1.5 x their waves is below the waves of 128-feature tiles."""
+    if T <= 256 and n_slots == 1:
+        return ["gemm_lora_kernel"]
     m_tiles = (H + 127) // 128
     n_tiles = (T + 255) // 256
     want = (3 * n_sm // 4 + m_tiles - 1) // m_tiles
@@ -222,7 +225,14 @@ def gemm_kernel_name(H, T, n_sm):
         n_tiles = min(want, (T + 31) // 32)
     bn = min(256, ((T + n_tiles - 1) // n_tiles + 31) // 32 * 32)
     n_tiles = (T + bn - 1) // bn
-    return "gemm_lora_persistent" if m_tiles * n_tiles > n_sm else "gemm_lora_kernel"
+    if n_slots == 1 and m_tiles * n_tiles <= n_sm:
+        return ["gemm_lora_kernel"]
+    mh = 1
+    if bn == 256:
+        w1 = -(-n_slots * m_tiles * n_tiles // n_sm)
+        w2 = -(-n_slots * ((H + 255) // 256) * n_tiles // n_sm)
+        mh = 2 if 3 * w2 < 2 * w1 else 1
+    return [f"gemm_lora_persistent<{mh}>"]
 
 
 # ------------------------------------------------------------------------------- our arm
@@ -569,8 +579,9 @@ def run_ours(args):
     shares = {k: v / max(1e-12, sum(res["kern_ms"].values())) for k, v in res["kern_ms"].items()}
     # The roofline object describes the kernel kind with the largest share of device time: the
     # base GEMM (its roof follows the workload's arithmetic intensity) or the LoRA delta (HBM).
-    # A kind may run as two kernels in one step (a grouped launch for q/k/v, a single one for o):
-    # its figures are then per-launch averages, algorithmic bytes and time alike.
+    # A kind runs as several kernels in one step (a grouped launch for q/k/v, one for o):
+    # its figures are per-launch averages, algorithmic bytes and time alike (the step's totals
+    # divided by the kernel launches the library counted; x is counted once per call).
     dominant = "delta" if res["kern_ms"]["delta"] > res["kern_ms"]["gemm"] else "gemm"
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     launch_ms = per_launch_ms[dominant]
@@ -578,7 +589,8 @@ def run_ours(args):
         kernel_file = os.path.join(ROOT, "adapter_gemm_lora_gb300", "csrc", "gemm_tcgen05.cu")
         kernel_name = gemm_kernel_names(wl, torch.cuda.get_device_properties(device).multi_processor_count)
         hbm_bound = alg["gemm_flops"] / alg["gemm_bytes"] < ridge
-        alg_bytes, alg_flops = alg["gemm_bytes"], alg["gemm_flops"]
+        n_launch = max(1, res["launches_per_step"]["gemm"])
+        alg_bytes, alg_flops = alg["gemm_bytes_step"] // n_launch, alg["gemm_flops_step"] // n_launch
     else:
         kernel_file = os.path.join(ROOT, "adapter_gemm_lora_gb300", "csrc", "lora_gather.cu")
         kernel_name = "lora_delta_kernel"

@@ -112,3 +112,14 @@ def test_gpus_flag_relaunches_or_checks_the_world(monkeypatch):
         bench.check_world(2, [])
     with pytest.raises(SystemExit):
         bench.check_world(0, [])
+
+
+def test_gemm_kernel_names_restate_the_tile_choice():
+    """The layer stack's q/k/v group (2,496 tokens, H = 5120) runs 256-feature tiles and its o
+    projection 128-feature ones (200 tiles of 256 features would leave the second wave nearly
+    empty); a decode batch of one slot takes the split-K kernel."""
+    import bench
+    assert bench.gemm_kernel_name(5120, 2496, 152, 3) == ["gemm_lora_persistent<2>"]
+    assert bench.gemm_kernel_name(5120, 2496, 152, 1) == ["gemm_lora_persistent<1>"]
+    assert bench.gemm_kernel_name(4096, 256, 152, 1) == ["gemm_lora_kernel"]
+    assert bench.gemm_kernel_name(4096, 9553, 152, 1) == ["gemm_lora_persistent<2>"]

@@ -97,6 +97,7 @@ FUSED = [
     (1024, [1500, 1200, 2000, 640], 300, [16, 64, 8, 40, 3], [0, 1]),     # a decode prefix: unfused tiles too
     (4096, [700, 1000], 0, [64, 16], [0, 1, 2, 3]),                       # group of four, K of 64 blocks
     (1344, [1500, 2000, 1500], 0, [16, 64, 8], [0, 1, 2]),               # 256-feature tiles, ragged last one
+    (5120, [512, 512, 512, 512], 448, [8, 16, 32, 64], [0]),            # one slot, a decode prefix, 128-feature tiles
 ]
 
 
