@@ -807,15 +807,46 @@ def main(argv=None):
                     help="layer stack only: keep its first N layers (profiling a stack-shaped step)")
     ap.add_argument("--prefetch", action="store_true",
                     help="also measure decode steps with adapter loads on a copy stream")
+    ap.add_argument("--eager-steps", type=int, default=0,
+                    help="for profilers: run this many untimed eager steps of the workload and exit")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="for profilers: run the attention leg alone (no workload) and print its figures")
+    ap.add_argument("--attention-requests", type=int, default=256)
+    ap.add_argument("--attention-h", type=int, default=0, help="attention leg hidden size (default: the workload's)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     rc = check_world(args.gpus, argv)
     if rc is not None:
         raise SystemExit(rc)
-    if args.impl == "reference":
+    if args.attention_only or args.eager_steps > 0:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
+
+
+def run_profile_case(args):
+    """Small, untimed runs for a profiler to capture: the workload's steps launched eagerly (one
+    segment build and every slot's projections per step), or the attention leg alone."""
+    import torch
+    device = torch.device("cuda", 0)
+    if args.attention_only:
+        import adapter_gemm_lora_gb300 as L
+        from adapter_gemm_lora_gb300 import build as B
+        B.build()
+        H = args.attention_h or workloads.SPECS[args.config].H
+        print(json.dumps(attention_leg(L, H, device, n_req=args.attention_requests, calls=2)), flush=True)
+        return
+    overrides = stack_layers(args.layers) if args.config == 5 and args.layers else None
+    h = Harness(args.config, device, overrides)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    for _ in range(args.eager_steps):
+        h.step(stream)
+    torch.cuda.synchronize()
+    h.L.lora_status(h.pool)
+    print(json.dumps({"profile_case": h.wl.spec.name, "steps": args.eager_steps, "T": h.wl.T, "H": h.wl.H,
+                      "pool_gb": round(h.pool_t.numel() * 2 / 1e9, 2)}), flush=True)
 
 
 if __name__ == "__main__":
