@@ -68,6 +68,23 @@ def test_segments_bit_exact(L, case):
     sc.close()
 
 
+def test_segments_at_the_adapter_id_limit_after_a_small_pool(L):
+    """The segment build keys its shared-memory histogram by adapter id, so a pool with
+    max_adapters = LORA_MAX_ADAPTERS needs 2 x 16,385 int32 of dynamic shared memory: a build on a
+    small pool first, then one on a pool at the limit (ids up to 16,383), both bit-exact."""
+    for n_ad, loaded in ((40, [0, 3, 39]), (L.LORA_MAX_ADAPTERS, [0, 7, 5000, L.LORA_MAX_ADAPTERS - 1])):
+        rng = np.random.default_rng(n_ad)
+        wl = workloads.small(H=64, T=600, n_adapters=n_ad, ranks=[8] * n_ad, seed=9)
+        sc = DeviceScene(L, wl, adapters=loaded)
+        ta = rng.choice(np.array(loaded + [-1], dtype=np.int32), size=600)
+        sc.segments(ta)
+        perm, off, sa = sc.read_segments()
+        w_perm, w_off, w_sa = O.segments(ta)
+        assert np.array_equal(perm, w_perm) and np.array_equal(off, w_off) and np.array_equal(sa, w_sa)
+        L.lora_status(sc.pool)
+        sc.close()
+
+
 def test_unknown_adapter_raises_device_error_and_is_treated_as_none(L):
     wl = workloads.small(H=128, T=16, n_adapters=4, ranks=[4, 8, 2, 16], seed=3)
     sc = DeviceScene(L, wl, adapters=[0, 1, 3])          # adapter 2 never loaded
