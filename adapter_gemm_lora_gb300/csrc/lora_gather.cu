@@ -18,11 +18,12 @@
 // are exchanged through distributed shared memory and added in cluster-rank order, so every CTA
 // holds the same complete s.  The expand then writes the CTA's share of delta.
 //
-// Data movement: one producer warp streams page-row slices (at most 1024 features, 2 KB) with
-// TMA bulk copies (cp.async.bulk): the unit's x rows into a buffer of their own, held across the
-// shrink, and the A pages, then the B pages, into a ring of 2 stages of 32 rows (two groups of 16
-// rank columns), each lane copying one row.  Up to 64 page rows and 16 x rows are in flight per
-// SM, without register staging.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
+// Data movement: one producer warp streams page-row slices with TMA bulk copies (cp.async.bulk):
+// the unit's x rows into a buffer of their own, held across the shrink, and the A pages, then the
+// B pages, into a ring of stages, each lane copying one row.  Feature blocks of 1024 (2 KB
+// slices): 2 stages of 32 rows (two groups of 16 rank columns).  A CTA share of 1280 features
+// (H = 5120, 4 CTAs) is one block of 2.5 KB slices instead of 1024 + 256: 3 stages of 16 rows.
+// The x buffer and the ring take the same shared memory either way.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
 // level bf16 MMA (m16n8k16, fp32 accumulation), feeding operands with ldmatrix straight from
 // the staged page rows: a unit holds 16 tokens at most, below the 64-row minimum tile of the
 // asynchronous tcgen05 MMA, while ldmatrix takes any row addresses, which is what a page
@@ -41,22 +42,30 @@
 namespace {
 
 constexpr int kUnitTok = kUnitTokens;         // tokens per unit (16)
-constexpr int kFB = 1024;                      // features per stage row (one feature block)
-constexpr int kRows = 32;                      // page rows per ring stage: two groups of 16
-constexpr int kStages = 2;                     // ring stages
 constexpr int kXRows = kUnitTok;               // x rows of the unit: a buffer of their own
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;      // + one producer warp
-// Staged rows are padded by 16 bytes so that the 8 rows an ldmatrix phase reads fall in 8
-// different 16-byte bank groups.
-constexpr int kRowBytes = kFB * 2 + 16;
-constexpr int kSlotBytes = kRows * kRowBytes;
 constexpr int kSbPitch = LORA_MAX_RANK + 8;    // bf16 elements per token row of s (hi or lo)
-// shared memory layout (dynamic)
+constexpr int kMaxStages = 3;
+// Ring geometry for feature blocks of FBW features.  Staged rows are padded by 16 bytes so that
+// the 8 rows an ldmatrix phase reads fall in 8 different 16-byte bank groups.
+template <int FBW>
+struct Ring {
+  static constexpr int kGroups = FBW > 1024 ? 1 : 2;          // groups of 16 rank columns a stage
+  static constexpr int kRows = 16 * kGroups;                  // page rows per stage
+  static constexpr int kRowBytes = FBW * 2 + 16;
+  static constexpr int kSlotBytes = kRows * kRowBytes;
+  static constexpr int kStages = FBW > 1024 ? 3 : 2;
+  static constexpr int kOffX = kStages * kSlotBytes;          // [16 tokens][kRowBytes] after the ring
+  static constexpr int kMT = FBW / 16 / kConsumerWarps;       // expand: 16-feature tiles per warp
+  static_assert(kStages <= kMaxStages && FBW % (16 * kConsumerWarps) == 0, "ring geometry");
+};
+// shared memory layout (dynamic): the ring and the x buffer in one area, then the rest
+constexpr int kAreaBytes = Ring<1024>::kOffX + kXRows * Ring<1024>::kRowBytes;
+static_assert(Ring<1280>::kOffX + kXRows * Ring<1280>::kRowBytes <= kAreaBytes, "ring area");
 constexpr int kOffRing = 0;
-constexpr int kOffX = kOffRing + kStages * kSlotBytes;                       // [16 tokens][kRowBytes]
-constexpr int kOffPart = kOffX + kXRows * kRowBytes;                         // [8 warps][16][16] f32
+constexpr int kOffPart = kAreaBytes;                                         // [8 warps][16][16] f32
 static_assert(kUnitTok == 16, "the MMA tiling assumes 16 tokens per unit");
 // The rest of the layout depends on the number KC of CTAs that split an item's features.
 template <int KC>
@@ -64,7 +73,7 @@ struct Smem {
   static constexpr int kOffExch = kOffPart + kConsumerWarps * 16 * 16 * 4;                 // [2][KC][64][16] f32
   static constexpr int kOffSb = kOffExch + 2 * KC * LORA_MAX_RANK * kUnitTok * 4;          // [2][16][kSbPitch] bf16
   static constexpr int kOffBar = kOffSb + 2 * kUnitTok * kSbPitch * 2;
-  static constexpr int kBytes = kOffBar + (2 * kStages + 4) * 8;
+  static constexpr int kBytes = kOffBar + (2 * kMaxStages + 4) * 8;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
   static_assert(kOffSb % 16 == 0 && kOffBar % 8 == 0, "alignment");
 };
@@ -230,10 +239,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_
                : "memory");
 }
 
-template <int KC>
+// FBW: features per block (1024, or 1280 for a 1280-feature share).  Nine warps put three on one
+// SM sub-partition, which caps a thread at 168 registers.
+template <int KC, int FBW>
 __global__ void __launch_bounds__(kThreads, 1)
 lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   constexpr int kCluster = KC;                            // CTAs per item, one feature share each
+  using R = Ring<FBW>;
+  constexpr int kFB = FBW, kRows = R::kRows, kStages = R::kStages, kGps = R::kGroups, kMT = R::kMT;
+  constexpr int kRowBytes = R::kRowBytes, kSlotBytes = R::kSlotBytes, kOffX = R::kOffX;
   using SM = Smem<KC>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -243,8 +257,8 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   float* exch = reinterpret_cast<float*>(smem + SM::kOffExch);
   __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(smem + SM::kOffSb);
   const uint32_t bar_full = smem_u32(smem + SM::kOffBar);
-  const uint32_t bar_empty = bar_full + 8 * kStages;
-  const uint32_t bar_exch = bar_empty + 8 * kStages;
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t bar_exch = bar_empty + 8 * kMaxStages;
   const uint32_t bar_xfull = bar_exch + 16, bar_xempty = bar_xfull + 8;
   const uint32_t xbuf = smem_u32(smem + kOffX);
 
@@ -300,9 +314,9 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             G.pa[h] = G.pb[h] = -1;                       // the column is dropped on both sides
           }
         }
-        const int nq = (U.r + 31) / 32;                   // stages of up to 32 rank columns
+        const int nq = (U.r + kRows - 1) / kRows;         // stages of up to kRows rank columns
         // in consumption order: per feature block, the x rows (own buffer) then the A stages;
-        // then the B stages.  Lane l copies rank column 32q + l of stage q.
+        // then the B stages.  Lane l < kRows copies rank column kRows q + l of stage q.
         for (int phase = 0; phase < 2 && ok; ++phase) {
           for (int fb = 0; fb < n_fb && ok; ++fb) {
             const int fw = min(kFB, Hq - fb * kFB);
@@ -321,8 +335,12 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
               const int s = it % kStages;
               ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1));
               if (!ok) break;
-              const int32_t page = q ? (phase == 0 ? G.pa[1] : G.pb[1]) : (phase == 0 ? G.pa[0] : G.pb[0]);
-              const bool mine = page >= 0;
+              // rank column j = kRows q + l is held by lane j % 32 in its entry j / 32 (the lane itself
+              // when a stage is 32 columns)
+              const int j0 = kRows * q;
+              const int32_t held = (j0 >> 5) ? (phase == 0 ? G.pa[1] : G.pb[1]) : (phase == 0 ? G.pa[0] : G.pb[0]);
+              const int32_t page = kRows == 32 ? held : __shfl_sync(0xffffffffu, held, (j0 + lane) & 31);
+              const bool mine = lane < kRows && page >= 0;
               const uint32_t rows = __popc(__ballot_sync(0xffffffffu, mine));
               if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, rows * fw * 2);
               __syncwarp();
@@ -372,7 +390,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
 
         // ---- shrink over this CTA's feature quarter: acc[n-tile] = A_g^T x^T (16 pages x 8 tokens)
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int nq = (U.r + 31) / 32;
+        const int nq = (U.r + kRows - 1) / kRows;
         for (int fb = 0; fb < n_fb; ++fb) {
           const int fw = min(kFB, Hq - fb * kFB);
           ok = ok && wait_warp(bar_xfull, xi & 1);
@@ -381,8 +399,8 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             const int s = it % kStages;
             ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
             ++it;
-            if (ok && (my_g >> 1) == q && my_g < ng) {   // this warp's group: rows 16*(my_g&1) ..
-              const uint32_t abase = ring + s * kSlotBytes + (my_g & 1) * 16 * kRowBytes;
+            if (ok && my_g / kGps == q && my_g < ng) {   // this warp's group: rows 16 (my_g % kGps) ..
+              const uint32_t abase = ring + s * kSlotBytes + (my_g % kGps) * 16 * kRowBytes;
               const uint32_t a_row = abase + (ri + 8 * (mi & 1)) * kRowBytes + 16 * (mi >> 1);
               const uint32_t x_row = xbuf + (ri + 8 * (mi >> 1)) * kRowBytes + 16 * (mi & 1);
 #pragma unroll 4
@@ -445,13 +463,13 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
         }
         consumer_sync();
 
-        // ---- expand: delta[t][f] for this CTA's features, warp w owns 128 features per block
+        // ---- expand: delta[t][f] for this CTA's features, warp w owns 16 kMT features per block
         for (int fb = 0; fb < n_fb; ++fb) {
           const int fw = min(kFB, Hq - fb * kFB);
-          const int f_warp = warp * 128;
-          float e[8][2][4];
+          const int f_warp = warp * 16 * kMT;
+          float e[kMT][2][4];
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -460,7 +478,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
             const int s = it % kStages;
             ok = ok && wait_warp(bar_full + 8 * s, (it / kStages) & 1);
             ++it;
-            for (int g = 2 * q; g < min(ng, 2 * q + 2) && ok && f_warp < fw; ++g) {
+            for (int g = kGps * q; g < min(ng, kGps * q + kGps) && ok && f_warp < fw; ++g) {
               uint32_t sh[4], sl[4];
               const uint32_t s_off = ((ri + 8 * (mi >> 1)) * kSbPitch + 16 * g + 8 * (mi & 1)) * 2;
               ldsm_x4(smem_u32(sb_hi) + s_off, sh);
@@ -469,9 +487,10 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
               const uint32_t kb = 16 * g + 2 * (lane & 3);
               const uint32_t m01 = (((vm >> kb) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 1)) & 1) ? 0xFFFF0000u : 0u);
               const uint32_t m23 = (((vm >> (kb + 8)) & 1) ? 0x0000FFFFu : 0u) | (((vm >> (kb + 9)) & 1) ? 0xFFFF0000u : 0u);
-              const uint32_t b_row = ring + s * kSlotBytes + ((g & 1) * 16 + ri + 8 * (mi >> 1)) * kRowBytes + 16 * (mi & 1);
+              const uint32_t b_row =
+                  ring + s * kSlotBytes + ((g % kGps) * 16 + ri + 8 * (mi >> 1)) * kRowBytes + 16 * (mi & 1);
 #pragma unroll
-              for (int mt = 0; mt < 8; ++mt) {
+              for (int mt = 0; mt < kMT; ++mt) {
                 if (f_warp + mt * 16 < fw) {
                   uint32_t af[4];
                   ldsm_x4_t(b_row + (f_warp + mt * 16) * 2, af);
@@ -493,7 +512,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
           // store the valid tokens' rows of delta
           const int fbase = f_cta + fb * kFB + f_warp + (lane >> 2);
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
+          for (int mt = 0; mt < kMT; ++mt) {
             if (f_warp + mt * 16 < fw) {
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt)
@@ -514,7 +533,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
   cluster_sync_all();                                     // no CTA leaves while a peer may still address it
 }
 
-template <int KC>
+template <int KC, int FBW>
 int active_clusters() {
   static int cached[kMaxDeviceFlags] = {0};
   int dev = 0;
@@ -533,7 +552,7 @@ int active_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, lora_delta_kernel<KC>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, lora_delta_kernel<KC, FBW>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = device_sm_count() / KC;
   }
@@ -541,13 +560,14 @@ int active_clusters() {
   return n;
 }
 
-template <int KC>
+template <int KC, int FBW>
 int launch_delta_kc(const LoraLaunch& L, cudaStream_t st) {
   static DeviceFlags attr;
-  int rc = ensure_smem_attr(attr, lora_delta_kernel<KC>, Smem<KC>::kBytes, "lora_delta_kernel: shared memory attribute");
+  int rc = ensure_smem_attr(attr, lora_delta_kernel<KC, FBW>, Smem<KC>::kBytes,
+                            "lora_delta_kernel: shared memory attribute");
   if (rc != LORA_OK) return rc;
   // Persistent clusters, as many as can be resident; each loops over the units.
-  int groups = active_clusters<KC>();
+  int groups = active_clusters<KC, FBW>();
   const int item_cap = L.seg->unit_cap * L.n_group;
   if (item_cap < groups) groups = item_cap > 0 ? item_cap : 1;
   cudaLaunchConfig_t cfg = {};
@@ -564,7 +584,7 @@ int launch_delta_kc(const LoraLaunch& L, cudaStream_t st) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = L.pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_delta_kernel<KC>, L, *L.seg);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lora_delta_kernel<KC, FBW>, L, *L.seg);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? LORA_OK : lora_cuda_fail(e, "lora_delta_kernel launch");
 }
@@ -572,11 +592,13 @@ int launch_delta_kc(const LoraLaunch& L, cudaStream_t st) {
 }  // namespace
 
 // The feature split of an item: 2 CTAs when their halves are at most 1024 features (H <= 2048:
-// twice as many items run at once), else 4.  A split into 5 (H = 5120: one 2 KB slice per page
-// row instead of a 2 KB and a 512 B one) made the kernel alone faster but a layer's chain of
-// kernels slower: its 150 SMs leave no room for the next kernel to start early.
+// twice as many items run at once), else 4.  A split into 5 made the kernel alone faster but a
+// layer's chain of kernels slower: its 150 SMs leave no room for the next kernel to start early.
 int delta_split(int32_t H) { return H <= 2048 ? 2 : 4; }
 
+// Feature blocks of 1024, except a CTA share of 1025..1280 features, which is one block.
 int launch_lora_delta(const LoraLaunch& L, cudaStream_t st) {
-  return delta_split(L.H) == 2 ? launch_delta_kc<2>(L, st) : launch_delta_kc<4>(L, st);
+  if (delta_split(L.H) == 2) return launch_delta_kc<2, 1024>(L, st);
+  const int Hq = L.H / 4;
+  return Hq > 1024 && Hq <= 1280 ? launch_delta_kc<4, 1280>(L, st) : launch_delta_kc<4, 1024>(L, st);
 }
