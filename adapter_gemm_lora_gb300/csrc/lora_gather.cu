@@ -23,12 +23,14 @@
 // B pages, into a ring of stages, each lane copying one row.  Feature blocks of 1024 (2 KB
 // slices): 2 stages of 32 rows (two groups of 16 rank columns).  A CTA share of 1280 features
 // (H = 5120, 4 CTAs) is one block of 2.5 KB slices instead of 1024 + 256: 3 stages of 16 rows.
-// The x buffer and the ring take the same shared memory either way.  Eight consumer warps multiply what has landed on the tensor cores with the warp-
-// level bf16 MMA (m16n8k16, fp32 accumulation), feeding operands with ldmatrix straight from
-// the staged page rows: a unit holds 16 tokens at most, below the 64-row minimum tile of the
-// asynchronous tcgen05 MMA, while ldmatrix takes any row addresses, which is what a page
-// gather produces.  The MMAs exist only to keep the 16-way reuse of every loaded byte off the
-// CUDA cores; the kernel is bound by the bytes it gathers.
+// The x buffer and the ring take the same shared memory either way.
+// Eight consumer warps multiply what has landed on the tensor cores with the warp-level bf16 MMA
+// (m16n8k16, fp32 accumulation), feeding operands with ldmatrix straight from the staged page
+// rows: a unit holds 16 tokens at most, below the 64-row minimum tile of the asynchronous
+// tcgen05 MMA, while ldmatrix takes any row addresses, which is what a page gather produces.
+// The MMAs exist only to keep the 16-way reuse of every loaded byte off the CUDA cores; the
+// kernel is bound by moving the bytes it gathers, through a fixed chain per item (x rows,
+// shrink, exchange, expand, stores).
 //
 // Precision: bf16 inputs, exact products, fp32 accumulation.  s is passed to the expand as
 // two bf16 terms (s = hi + lo, with hi = bf16(s), lo = bf16(s - hi)), which keeps 16 bits of
@@ -388,7 +390,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
         const int wpg = kConsumerWarps / ng;              // warps per page group in the shrink
         const int my_g = warp / wpg, sub = warp % wpg;
 
-        // ---- shrink over this CTA's feature quarter: acc[n-tile] = A_g^T x^T (16 pages x 8 tokens)
+        // ---- shrink over this CTA's feature share: acc[n-tile] = A_g^T x^T (16 pages x 8 tokens)
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int nq = (U.r + kRows - 1) / kRows;
         for (int fb = 0; fb < n_fb; ++fb) {
@@ -431,7 +433,7 @@ lora_delta_kernel(LoraLaunch L, lora_segments seg) {
           }
         }
         consumer_sync();
-        // This CTA's partial of s over its quarter goes to all four CTAs, exch[b][q][j][t], as
+        // This CTA's partial of s over its share goes to all KC CTAs, exch[b][q][j][t], as
         // asynchronous remote stores that count their bytes on the receiver's barrier.
         const int b = n_done & 1;
         if (tid == 0) mbar_arrive_expect_tx(bar_exch + 8 * b, kCluster * ng * 256 * 4);
