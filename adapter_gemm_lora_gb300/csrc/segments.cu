@@ -6,11 +6,13 @@
 // token.  Output order: ascending adapter id, ties by token index; tokens without an
 // adapter (-1) first and outside every segment.
 //
-// One CTA of 1024 threads: a shared-memory histogram over adapter ids (with each used
-// adapter's rank), two block scans that turn counts into run starts, segment indices and the
-// offsets of the LoRA-delta work units within their rank class (each unit written right away
-// as a complete record: adapter, rank, first index into perm, token count), then a stable
-// scatter in chunks of 1024 tokens (warp-level match for ranks inside a warp, warps in order).
+// One CTA of 1024 threads: a shared-memory histogram over adapter ids (the rank table is
+// read into shared memory beside it, while the first 1024 ids are in flight), one block scan
+// that turns counts into run starts, segment indices and the offsets of the LoRA-delta work
+// units within their rank class (each unit written right away as a complete record: adapter,
+// rank, first index into perm, token count), then a stable scatter in chunks of 1024 tokens
+// (warp-level match for ranks inside a warp, warps in order; the first chunk's keys stay in
+// registers).
 #include <cuda_runtime.h>
 
 #include "lora_internal.h"
@@ -28,12 +30,16 @@ __device__ __forceinline__ void flag_error(int32_t* err, int32_t bits) {
 // Work-unit cost class of a rank: 0 for 33..64, 1 for 17..32, 2 for 9..16, 3 for 1..8.
 __device__ __forceinline__ int rank_class(int32_t r) { return r > 32 ? 0 : r > 16 ? 1 : r > 8 ? 2 : 3; }
 
-// Exclusive block scan of four int32 values per thread; totals land in tot[0..3].
-__device__ __forceinline__ void block_exclusive_scan4(int32_t (&v)[4], int32_t (*sh)[33], int32_t (&tot)[4]) {
+constexpr int kScanMax = 6;   // values per thread in one block scan, at most
+
+// Exclusive block scan of N int32 values per thread; totals land in tot[0..N-1].
+template <int N>
+__device__ __forceinline__ void block_exclusive_scan(int32_t (&v)[N], int32_t (*sh)[33], int32_t (&tot)[N]) {
+  static_assert(N <= kScanMax, "scan scratch holds kScanMax rows");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int32_t inc[4];
+  int32_t inc[N];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < N; ++q) {
     inc[q] = v[q];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -45,7 +51,7 @@ __device__ __forceinline__ void block_exclusive_scan4(int32_t (&v)[4], int32_t (
   __syncthreads();
   if (warp == 0) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < N; ++q) {
       const int32_t w = sh[q][lane];
       int32_t x = w;
 #pragma unroll
@@ -59,7 +65,7 @@ __device__ __forceinline__ void block_exclusive_scan4(int32_t (&v)[4], int32_t (
   }
   __syncthreads();
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < N; ++q) {
     v[q] = sh[q][warp] + inc[q] - v[q];
     tot[q] = sh[q][32];
   }
@@ -72,57 +78,55 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                          // [K] tokens per key, then run starts / write cursors
   int32_t* krank = sm + (max_adapters + 1);   // [K] rank of the key's adapter
-  __shared__ int32_t sh_scan[4][33];
+  __shared__ int32_t sh_scan[kScanMax][33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = max_adapters + 1;              // key = adapter id + 1; key 0 = no adapter
   pdl_wait_then_release();
 
-  for (int k = tid; k < K; k += kThreads) cnt[k] = 0;
+  const int32_t a_first = tid < T ? token_adapter[tid] : -1;   // in flight while the tables fill
+  for (int k = tid; k < K; k += kThreads) {
+    cnt[k] = 0;
+    krank[k] = k > 0 ? rank[k - 1] : 0;
+  }
   __syncthreads();
 
-  // 1. validate ids, count tokens per key, remember each used adapter's rank
+  // 1. validate ids, count tokens per key
+  int32_t key_first = 0;                       // key of token tid, kept for the scatter
   for (int t = tid; t < T; t += kThreads) {
-    const int32_t a = token_adapter[t];
+    const int32_t a = t == tid ? a_first : token_adapter[t];
     int32_t key = 0;
     if (a >= 0 && a < max_adapters) {
-      const int32_t r = rank[a];
-      if (r > 0) {
-        key = a + 1;
-        krank[key] = r;
-      } else {
-        flag_error(err, LORA_DEV_UNKNOWN_ADAPTER);
-      }
+      if (krank[a + 1] > 0) key = a + 1;
+      else flag_error(err, LORA_DEV_UNKNOWN_ADAPTER);
     } else if (a != -1) {
       flag_error(err, LORA_DEV_UNKNOWN_ADAPTER);
     }
+    if (t == tid) key_first = key;
     seg.tok_adapter[t] = key - 1;
     atomicAdd(&cnt[key], 1);
   }
   __syncthreads();
 
-  // 2. one scan gives run starts and segment indices, a second one the work-unit offsets
-  //    inside each rank class; each thread then writes the segments and work units of its own
-  //    keys.  Units are listed by rank class, largest ranks first (a unit's cost grows with
-  //    the pages it gathers), then by adapter id and token offset, so that the delta kernel,
-  //    which deals units to its clusters in waves, starts the longest ones first.
+  // 2. one scan gives run starts, segment indices and the work-unit offsets inside each rank
+  //    class; each thread then writes the segments and work units of its own keys.  Units are
+  //    listed by rank class, largest ranks first (a unit's cost grows with the pages it
+  //    gathers), then by adapter id and token offset, so that the delta kernel, which deals
+  //    units to its clusters in waves, starts the longest ones first.
   const int per = (K + kThreads - 1) / kThreads;
   const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
-  int32_t v[4] = {0, 0, 0, 0};                 // tokens, segments, -, -
-  int32_t ub[4] = {0, 0, 0, 0};                // work units per rank class
+  int32_t v[6] = {0, 0, 0, 0, 0, 0};           // tokens, segments, work units per rank class
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     v[0] += c;
     if (k > 0 && c > 0) {
       v[1] += 1;
-      ub[rank_class(krank[k])] += (c + kUnitTokens - 1) / kUnitTokens;
+      v[2 + rank_class(krank[k])] += (c + kUnitTokens - 1) / kUnitTokens;
     }
   }
-  int32_t tot[4], utot[4];
-  block_exclusive_scan4(v, sh_scan, tot);
-  block_exclusive_scan4(ub, sh_scan, utot);
-  ub[1] += utot[0];
-  ub[2] += utot[0] + utot[1];
-  ub[3] += utot[0] + utot[1] + utot[2];
+  int32_t tot[6];
+  block_exclusive_scan(v, sh_scan, tot);
+  const int32_t utot[4] = {tot[2], tot[3], tot[4], tot[5]};
+  int32_t ub[4] = {v[2], v[3] + utot[0], v[4] + utot[0] + utot[1], v[5] + utot[0] + utot[1] + utot[2]};
   for (int k = k_lo; k < k_hi; ++k) {
     const int32_t c = cnt[k];
     if (k > 0 && c > 0) {
@@ -152,7 +156,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   for (int base_t = 0; base_t < T; base_t += kThreads) {
     const int t = base_t + tid;
     const bool valid = t < T;
-    const int32_t key = valid ? seg.tok_adapter[t] + 1 : -1;
+    const int32_t key = !valid ? -1 : base_t == 0 ? key_first : seg.tok_adapter[t] + 1;
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     const int lrank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
@@ -221,7 +225,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
   }
   for (int i = n_tiles + tid; i < seg.n_tiles_max; i += kThreads) seg.tile_plan[(size_t)i * kPlanStride] = -1;
   int32_t etot[4];
-  block_exclusive_scan4(ev, sh_scan, etot);    // also orders the tile_cnt reads before the rewrite below
+  block_exclusive_scan(ev, sh_scan, etot);    // also orders the tile_cnt reads before the rewrite below
   if (tid < n_tiles) {
     for (int b = 0; b < nb; ++b) seg.entries[ev[0] + b] = tid * kTileAdapters + b;
     tile_cnt[tid] = nb;                        // from here on: < 0 marks a tile that is not fused
@@ -253,7 +257,7 @@ segments_kernel(const int32_t* __restrict__ token_adapter, int32_t T, const int3
     }
   }
   int32_t ltot[4];
-  block_exclusive_scan4(lv, sh_scan, ltot);
+  block_exclusive_scan(lv, sh_scan, ltot);
   for (int u = u_lo, pos = lv[0]; u < u_hi; ++u)
     if ((live_bits >> (u - u_lo)) & 1u) {
       int4 rec = reinterpret_cast<const int4*>(seg.units)[u];
