@@ -34,7 +34,8 @@ def _run_slot(sc, ta, slot, x_bits, W_bits, tokens=None):
 
 
 # ---------------------------------------------------------------------------- segments
-@pytest.mark.parametrize("case", ["random", "all_none", "all_distinct", "single", "one_token", "empty", "long"])
+@pytest.mark.parametrize("case", ["random", "all_none", "all_distinct", "single", "one_token", "empty", "long",
+                                  "chunk_exact", "chunk_plus_one"])
 def test_segments_bit_exact(L, case):
     rng = np.random.default_rng(zlib.crc32(case.encode()))
     n_ad = 40
@@ -44,7 +45,10 @@ def test_segments_bit_exact(L, case):
           "single": lambda: np.full(300, 7),
           "one_token": lambda: np.array([5]),
           "empty": lambda: np.zeros(0, dtype=np.int64),
-          "long": lambda: rng.integers(-1, n_ad, size=5000)}[case]().astype(np.int32)
+          "long": lambda: rng.integers(-1, n_ad, size=5000),
+          # the build handles 1,024 tokens per chunk and keeps the first chunk's keys in registers
+          "chunk_exact": lambda: rng.integers(-1, n_ad, size=1024),
+          "chunk_plus_one": lambda: rng.integers(-1, n_ad, size=1025)}[case]().astype(np.int32)
     ranks = [(3, 12, 24, 64, 8, 40, 17, 9)[a % 8] for a in range(n_ad)]     # every rank class
     wl = workloads.small(H=64, T=max(len(ta), 1), n_adapters=n_ad, ranks=ranks, seed=1)
     sc = DeviceScene(L, wl)
@@ -101,6 +105,29 @@ def test_unknown_adapter_raises_device_error_and_is_treated_as_none(L):
     y, d, y_ref, d_ref = _run_slot(sc, ta_eff, 0, x, W)
     check_close(y, d, y_ref, d_ref, "unknown->none")
     L.lora_status(sc.pool)                               # cleared by the previous read
+    sc.close()
+
+
+def test_out_of_range_adapter_ids_are_flagged_and_treated_as_none(L):
+    """Ids below -1 or at and above max_adapters: the error word is raised, the tokens take no
+    LoRA term, and the segments are those of the batch with those ids replaced by -1 (in the
+    first 1,024-token chunk and after it)."""
+    wl = workloads.small(H=128, T=1100, n_adapters=4, ranks=[4, 8, 2, 16], seed=5)
+    sc = DeviceScene(L, wl)
+    rng = np.random.default_rng(17)
+    ta = rng.integers(-1, 4, size=1100).astype(np.int32)
+    bad = np.array([3, 100, 517, 1023, 1024, 1099])
+    ta[bad] = np.array([4, -2, 1 << 30, -(1 << 31), 5, 4], dtype=np.int32)
+    sc.segments(ta)
+    with pytest.raises(L.LoraError) as e:
+        L.lora_status(sc.pool)
+    assert e.value.code == L.LORA_EDEVICE and "unknown adapter" in e.value.message
+    ta_eff = ta.copy()
+    ta_eff[bad] = -1
+    perm, off, sa = sc.read_segments()
+    w = O.segments(ta_eff)
+    assert np.array_equal(perm, w[0]) and np.array_equal(off, w[1]) and np.array_equal(sa, w[2])
+    L.lora_status(sc.pool)
     sc.close()
 
 
